@@ -1,0 +1,164 @@
+"""NumPy float64 twin of the C oracle, and the tiled online-softmax recurrence.
+
+TEST INFRASTRUCTURE ONLY: imported by tests, the smoke check and the
+benchmark's CPU baseline, never by the product path.
+
+``attn_fwd_np`` / ``attn_decode_np`` compute the same plain definition as
+``attn_oracle.c`` but are written independently (vectorised NumPy, boolean
+masks instead of per-key branches), so that the two can be compared.
+
+``attn_tiled_online_np`` is the method itself, stated in float64: keys are
+processed in tiles while a running row maximum ``m`` and denominator ``l`` are
+kept, and earlier partial sums are rescaled by ``exp(m_old - m_new)`` whenever
+the maximum grows ("Implementing attention from scratch", Core ideas, Stable
+softmax; "Self-Attention: Implementation, Complexity, and Efficient
+Variants", Task 2 and Hint 1; "FlashAttention", section 9.4.1 and Figure
+9.8).  The NumPy build guide's Step 5 normalises each key tile on its own and
+adds the tiles together, which does not give softmax; the recurrence here is
+the reading its own Architecture Overview ("running max and sum of
+exponentials") and the other pages support.  It is used only to check
+"tiled == full", never as the oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+_NEG_INF = -np.inf
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of raw bfloat16 bit patterns (uint16) to float64."""
+    u32 = bits.astype(np.uint32) << np.uint32(16)
+    return u32.view(np.float32).astype(np.float64)
+
+
+def _as_f64(x: np.ndarray, bf16: bool) -> np.ndarray:
+    if bf16:
+        return bf16_bits_to_f64(np.asarray(x, dtype=np.uint16))
+    return np.asarray(x, dtype=np.float64)
+
+
+def visibility(T: int, S: int, L: int, causal: bool) -> tuple[np.ndarray, np.ndarray]:
+    """(row_valid [T], visible [T,S]) for one sequence.
+
+    Query row i sits at key position i + S - T (bottom-right alignment).  It is
+    a padded row when that position is >= L.  Key j is visible to row i when
+    j < L and, for causal attention, j <= i + S - T.
+    """
+    pos = np.arange(T)[:, None] + (S - T)
+    j = np.arange(S)[None, :]
+    vis = j < L
+    if causal:
+        vis = vis & (j <= pos)
+    row_valid = (np.arange(T) + (S - T)) < L
+    vis = vis & row_valid[:, None]
+    return row_valid, vis
+
+
+def attn_fwd_np(q, k, v, causal=False, key_lens=None, scale=None, bf16=False):
+    """Full-softmax attention in float64.  q [B,Hq,T,D], k/v [B,Hkv,S,D].
+
+    Returns (o [B,Hq,T,D], lse [B,Hq,T]); rows with no visible key (padded
+    rows included) are O = 0, LSE = -inf.
+    """
+    q, k, v = (_as_f64(x, bf16) for x in (q, k, v))
+    B, Hq, T, D = q.shape
+    _, Hkv, S, _ = k.shape
+    assert Hq % Hkv == 0
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    G = Hq // Hkv
+    o = np.zeros((B, Hq, T, D))
+    lse = np.full((B, Hq, T), _NEG_INF)
+    for b in range(B):
+        L = S if key_lens is None else int(key_lens[b])
+        _, vis = visibility(T, S, L, causal)
+        has = vis.any(axis=1)
+        for h in range(Hq):
+            g = h // G
+            s = (q[b, h] @ k[b, g].T) * scale
+            s = np.where(vis, s, _NEG_INF)
+            m = np.where(has, s.max(axis=1), 0.0)
+            e = np.where(vis, np.exp(s - m[:, None]), 0.0)
+            z = e.sum(axis=1)
+            zs = np.where(has, z, 1.0)
+            o[b, h] = (e / zs[:, None]) @ v[b, g]
+            lse[b, h] = np.where(has, m + np.log(zs), _NEG_INF)
+    return o, lse
+
+
+def attn_decode_np(q, kcache, vcache, kv_lens, scale=None, bf16=False):
+    """One query per (b, h) against the first kv_lens[b] cache rows.
+
+    q [B,Hq,D], caches [B,Hkv,S_max,D].  Returns (o [B,Hq,D], lse [B,Hq]).
+    """
+    q4 = np.asarray(q)[:, :, None, :]
+    q4 = _as_f64(q4, bf16)
+    kc, vc = _as_f64(kcache, bf16), _as_f64(vcache, bf16)
+    B, Hq, _, D = q4.shape
+    o = np.zeros((B, Hq, D))
+    lse = np.full((B, Hq), _NEG_INF)
+    for b in range(B):
+        L = int(kv_lens[b])
+        if L <= 0:
+            continue
+        # The single query sits at position L-1 and sees keys 0..L-1.
+        ob, lb = attn_fwd_np(q4[b:b + 1], kc[b:b + 1, :, :L], vc[b:b + 1, :, :L],
+                             causal=True, key_lens=None, scale=scale)
+        o[b] = ob[0, :, 0]
+        lse[b] = lb[0, :, 0]
+    return o, lse
+
+
+def attn_tiled_online_np(q, k, v, causal=False, key_lens=None, scale=None,
+                         tile_q=64, tile_k=64, bf16=False):
+    """The tiled method with an online softmax, in float64.
+
+    For every query tile, keys are visited tile by tile.  Per row it keeps the
+    running maximum m, the running denominator l and the unnormalised output
+    acc.  With the scores s of a new key tile:
+
+        m_new = max(m, rowmax(s))
+        acc   = acc * exp(m - m_new) + exp(s - m_new) @ V_tile
+        l     = l   * exp(m - m_new) + rowsum(exp(s - m_new))
+
+    and at the end O = acc / l, LSE = m + ln l.
+    """
+    q, k, v = (_as_f64(x, bf16) for x in (q, k, v))
+    B, Hq, T, D = q.shape
+    _, Hkv, S, _ = k.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    G = Hq // Hkv
+    o = np.zeros((B, Hq, T, D))
+    lse = np.full((B, Hq, T), _NEG_INF)
+    for b in range(B):
+        L = S if key_lens is None else int(key_lens[b])
+        _, vis = visibility(T, S, L, causal)
+        for h in range(Hq):
+            g = h // G
+            for q0 in range(0, T, tile_q):
+                q1 = min(q0 + tile_q, T)
+                n = q1 - q0
+                m = np.full(n, _NEG_INF)
+                l = np.zeros(n)
+                acc = np.zeros((n, D))
+                for k0 in range(0, S, tile_k):
+                    k1 = min(k0 + tile_k, S)
+                    s = (q[b, h, q0:q1] @ k[b, g, k0:k1].T) * scale
+                    tv = vis[q0:q1, k0:k1]
+                    s = np.where(tv, s, _NEG_INF)
+                    m_new = np.maximum(m, s.max(axis=1))
+                    # Rows that have seen no visible key yet keep a zero
+                    # reference so that exp() of -inf - -inf never appears.
+                    ref = np.where(np.isfinite(m_new), m_new, 0.0)
+                    alpha = np.where(np.isfinite(m), np.exp(m - ref), 0.0)
+                    p = np.where(tv, np.exp(s - ref[:, None]), 0.0)
+                    acc = acc * alpha[:, None] + p @ v[b, g, k0:k1]
+                    l = l * alpha + p.sum(axis=1)
+                    m = m_new
+                has = l > 0
+                ls = np.where(has, l, 1.0)
+                o[b, h, q0:q1] = np.where(has[:, None], acc / ls[:, None], 0.0)
+                lse[b, h, q0:q1] = np.where(has, m + np.log(ls), _NEG_INF)
+    return o, lse
