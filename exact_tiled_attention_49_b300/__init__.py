@@ -1,0 +1,22 @@
+"""Exact tiled attention for B300 (sm_103a).
+
+O = softmax(Q K^T * scale + mask) V computed tile by tile with an online
+softmax so that the score matrix never reaches HBM: a causal/padding-masked
+prefill forward with per-row log-sum-exp, a split-KV single-query decode step
+with GQA/MQA head sharing, and an O(1) KV-cache append.
+
+The work is done by hand-written CUDA kernels in ``libattn.so`` behind a C
+ABI (``include/attn.h``); this package is a thin ctypes binding of it.
+"""
+from ._lib import (ATTN_BF16, ATTN_ERR_CUDA, ATTN_ERR_INVALID_ARG,  # noqa: F401
+                   ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_F32, ATTN_OK,
+                   LIB_PATH, SIGNATURES, AttnError, attn_decode,
+                   attn_decode_workspace_size, attn_device_error, attn_fwd,
+                   attn_kernel_launches, attn_status_string, kv_cache_append, load,
+                   status_string)
+
+__all__ = [
+    "attn_fwd", "attn_decode", "attn_decode_workspace_size", "kv_cache_append",
+    "attn_status_string", "attn_kernel_launches", "attn_device_error", "AttnError",
+    "load", "LIB_PATH",
+]

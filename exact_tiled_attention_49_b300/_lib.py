@@ -1,0 +1,209 @@
+"""ctypes binding of libattn.so (argument marshalling only).
+
+Every function here validates Python-side types, turns torch tensors into
+device pointers and sizes, and calls the C entry point of the same name on
+the current CUDA stream.  All arithmetic runs in the library's CUDA kernels;
+there is no CPU or PyTorch fallback, and a missing library is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn.so")
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA = range(5)
+ATTN_F32, ATTN_BF16 = 0, 1
+
+# Every entry point declared in include/attn.h, with its ctypes signature.
+_P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+SIGNATURES = {
+    "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _F, _P]),
+    "attn_decode_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
+    "attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
+                         ctypes.c_size_t, _P]),
+    "kv_cache_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
+    "attn_status_string": (ctypes.c_char_p, [_I]),
+    "attn_kernel_launches": (ctypes.c_ulonglong, []),
+    "attn_device_error": (_I, [ctypes.POINTER(ctypes.c_int), _I]),
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it with `python -m exact_tiled_attention_49_b300.build`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().attn_status_string(int(status)).decode()
+
+
+def attn_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def _check(rc: int, what: str):
+    if rc != ATTN_OK:
+        raise AttnError(rc, what)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float32:
+        return ATTN_F32
+    raise TypeError(f"unsupported dtype {t.dtype}; expected bfloat16 or float32")
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def attn_fwd(q, k, v, o=None, lse=None, causal=False, key_lens=None, scale=None,
+             return_lse=True, stream=None):
+    """Prefill forward.  q [B,Hq,T,D], k/v [B,Hkv,S,D] (bf16 or fp32, CUDA).
+
+    Returns (o, lse): o like q, lse float32 [B,Hq,T] (None if return_lse is
+    False and no lse buffer was given).  key_lens: int32 CUDA [B] or None.
+    """
+    lib = load()
+    B, Hq, T, D = q.shape
+    Bk, Hkv, S, Dk = k.shape
+    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q/k/v shape mismatch")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    dt = _dtype_code(q)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, T), device=q.device, dtype=torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    ptrs = [_dev(q, "q", ndim=4), _dev(k, "k", ndim=4), _dev(v, "v", ndim=4),
+            _dev(o, "o", dtype=q.dtype, ndim=4)]
+    if tuple(o.shape) != tuple(q.shape):
+        raise ValueError("o must have q's shape")
+    lp = None
+    if lse is not None:
+        lp = _dev(lse, "lse", dtype=torch.float32)
+        if lse.numel() != B * Hq * T:
+            raise ValueError("lse must hold B*Hq*T floats")
+    kl = None
+    if key_lens is not None:
+        kl = _dev(key_lens, "key_lens", dtype=torch.int32, ndim=1)
+        if key_lens.numel() != B:
+            raise ValueError("key_lens must have B entries")
+    rc = lib.attn_fwd(*ptrs, lp, B, Hq, Hkv, T, S, D, dt, int(bool(causal)), kl,
+                      float(scale), _stream(stream))
+    _check(rc, "attn_fwd")
+    return o, lse
+
+
+def attn_decode_workspace_size(B: int, Hq: int, S_max: int, D: int) -> int:
+    return int(load().attn_decode_workspace_size(B, Hq, S_max, D))
+
+
+def attn_decode(q, kcache, vcache, kv_lens, o=None, lse=None, workspace=None,
+                scale=None, return_lse=True, stream=None):
+    """Decode step.  q [B,Hq,D], caches [B,Hkv,S_max,D], kv_lens int32 [B].
+
+    ``workspace`` (uint8 CUDA tensor) is allocated if not given.
+    Returns (o [B,Hq,D], lse [B,Hq] or None).
+    """
+    lib = load()
+    B, Hq, D = q.shape
+    Bk, Hkv, S_max, Dk = kcache.shape
+    if Bk != B or Dk != D or tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError("q/cache shape mismatch")
+    if kcache.dtype != q.dtype or vcache.dtype != q.dtype:
+        raise TypeError("q and the caches must share one dtype")
+    dt = _dtype_code(q)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), device=q.device, dtype=torch.float32)
+    need = attn_decode_workspace_size(B, Hq, S_max, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lp = _dev(lse, "lse", dtype=torch.float32) if lse is not None else None
+    rc = lib.attn_decode(_dev(q, "q", ndim=3), _dev(kcache, "kcache", ndim=4),
+                         _dev(vcache, "vcache", ndim=4),
+                         _dev(kv_lens, "kv_lens", dtype=torch.int32, ndim=1),
+                         _dev(o, "o", dtype=q.dtype, ndim=3), lp, B, Hq, Hkv, S_max, D, dt,
+                         float(scale), _dev(workspace, "workspace"),
+                         workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_decode")
+    return o, lse
+
+
+def kv_cache_append(kcache, vcache, k_new, v_new, pos, dev_status=None, stream=None):
+    """Write k_new/v_new [B,Hkv,D] at row pos[b] of the caches [B,Hkv,S_max,D]."""
+    lib = load()
+    B, Hkv, S_max, D = kcache.shape
+    if tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError("cache shape mismatch")
+    if tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D):
+        raise ValueError("k_new/v_new must be [B,Hkv,D]")
+    for t in (vcache, k_new, v_new):
+        if t.dtype != kcache.dtype:
+            raise TypeError("cache and new rows must share one dtype")
+    ds = _dev(dev_status, "dev_status", dtype=torch.int32) if dev_status is not None else None
+    rc = lib.kv_cache_append(_dev(kcache, "kcache"), _dev(vcache, "vcache"),
+                             _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+                             _dev(pos, "pos", dtype=torch.int32, ndim=1), B, Hkv, S_max, D,
+                             _dtype_code(kcache), ds, _stream(stream))
+    _check(rc, "kv_cache_append")
+
+
+def attn_kernel_launches() -> int:
+    return int(load().attn_kernel_launches())
+
+
+def attn_device_error(clear: bool = True) -> int:
+    code = ctypes.c_int(0)
+    _check(load().attn_device_error(ctypes.byref(code), int(bool(clear))), "attn_device_error")
+    return code.value

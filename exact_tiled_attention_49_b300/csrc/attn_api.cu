@@ -1,0 +1,314 @@
+// attn_api.cu -- host side of libattn.so: argument validation, TMA tensor-map
+// encoding and kernel dispatch behind the C ABI declared in include/attn.h.
+//
+// Everything is one translation unit so that the device error word and the
+// kernels need no relocatable device code.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "append.cuh"
+#include "common.cuh"
+#include "decode.cuh"
+#include "fwd_bf16_tc.cuh"
+#include "fwd_f32.cuh"
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxDevices = 64;
+
+std::atomic<unsigned long long> g_launches{0};
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// cuTensorMapEncodeTiled from the driver, resolved once through the runtime.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 3-D bf16 tensor [outer, rows, D] (D contiguous) loaded as boxes of
+// 64 columns x 128 rows with 128-byte swizzle; rows past `rows` read as 0.
+bool make_tmap_bf16(CUtensorMap* m, const void* base, int D, int rows, long long outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows * (cuuint64_t)D * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Opt a kernel into more than 48 KB of dynamic shared memory, once per device.
+template <typename K>
+bool ensure_smem(K kernel, size_t bytes, std::atomic<uint64_t>& done_mask) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  const uint64_t bit = 1ull << dev;
+  if (done_mask.load(std::memory_order_acquire) & bit) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+      cudaSuccess)
+    return false;
+  done_mask.fetch_or(bit, std::memory_order_acq_rel);
+  return true;
+}
+
+int launch_status() {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return cudaPeekAtLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// ------------------------------------------------------------- prefill
+
+template <int D>
+int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                  int Hq, int Hkv, int T, int S, int causal, const int32_t* key_lens,
+                  float scale, cudaStream_t st) {
+  using namespace attn::tcfwd;
+  static std::atomic<uint64_t> smem_done{0};
+  auto kernel = fwd_bf16_tc_kernel<D>;
+  if (!ensure_smem(kernel, Cfg<D>::kSmemAlloc, smem_done)) return ATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  if (!make_tmap_bf16(&tq, q, D, T, (long long)B * Hq) ||
+      !make_tmap_bf16(&tk, k, D, S, (long long)B * Hkv) ||
+      !make_tmap_bf16(&tv, v, D, S, (long long)B * Hkv))
+    return ATTN_ERR_CUDA;
+  Params p;
+  p.o = o;
+  p.lse = lse;
+  p.key_lens = key_lens;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.T = T;
+  p.S = S;
+  p.causal = causal ? 1 : 0;
+  p.n_qtiles = (T + kBM - 1) / kBM;
+  p.scale_log2 = scale * kLog2e;
+  dim3 grid(p.n_qtiles, Hq, B);
+  kernel<<<grid, kThreads, Cfg<D>::kSmemAlloc, st>>>(tq, tk, tv, p);
+  return launch_status();
+}
+
+template <int NC>
+int launch_fwd_f32(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int Hq, int Hkv, int T, int S, int D, int causal, const int32_t* key_lens,
+                   float scale, cudaStream_t st) {
+  using namespace attn::f32fwd;
+  static std::atomic<uint64_t> smem_done{0};
+  auto kernel = fwd_f32_kernel<NC>;
+  const size_t smem = smem_bytes(D);
+  if (!ensure_smem(kernel, smem_bytes(32 * NC), smem_done)) return ATTN_ERR_CUDA;
+  Params p;
+  p.q = static_cast<const float*>(q);
+  p.k = static_cast<const float*>(k);
+  p.v = static_cast<const float*>(v);
+  p.o = static_cast<float*>(o);
+  p.lse = lse;
+  p.key_lens = key_lens;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.T = T;
+  p.S = S;
+  p.D = D;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  dim3 grid((T + kBM - 1) / kBM, Hq, B);
+  kernel<<<grid, kWarps * 32, smem, st>>>(p);
+  return launch_status();
+}
+
+// -------------------------------------------------------------- decode
+
+template <typename T, int D, int G>
+int launch_decode_g(const attn::decode::Params& p, cudaStream_t st) {
+  using namespace attn::decode;
+  static std::atomic<uint64_t> smem_done{0};
+  auto kernel = decode_split_kernel<T, D, G>;
+  constexpr size_t smem = split_smem_bytes<T, D, G>();
+  if (!ensure_smem(kernel, smem, smem_done)) return ATTN_ERR_CUDA;
+  dim3 grid(p.splits, p.Hkv, p.B);
+  kernel<<<grid, kThreads, smem, st>>>(p);
+  int rc = launch_status();
+  if (rc != ATTN_OK) return rc;
+  decode_combine_kernel<T, D><<<dim3(p.Hq, p.B), D, 0, st>>>(p);
+  return launch_status();
+}
+
+template <typename T, int D>
+int launch_decode_d(const attn::decode::Params& p, int G, cudaStream_t st) {
+  switch (G) {
+    case 1: return launch_decode_g<T, D, 1>(p, st);
+    case 2: return launch_decode_g<T, D, 2>(p, st);
+    case 4: return launch_decode_g<T, D, 4>(p, st);
+    case 8: return launch_decode_g<T, D, 8>(p, st);
+    case 16: return launch_decode_g<T, D, 16>(p, st);
+    default: return ATTN_ERR_UNSUPPORTED;
+  }
+}
+
+bool finite_positive(float x) { return std::isfinite(x) && x > 0.f; }
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int T, int S, int D, int dtype, int causal, const int32_t* key_lens,
+             float scale, attn_stream_t stream) {
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || S <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !finite_positive(scale)) return ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (lse != nullptr && !aligned4(lse)) return ATTN_ERR_INVALID_ARG;
+  if (key_lens != nullptr && !aligned4(key_lens)) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == ATTN_BF16) {
+    if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
+      return ATTN_ERR_INVALID_ARG;
+    if (D == 64) return launch_fwd_tc<64>(q, k, v, o, lse, B, Hq, Hkv, T, S, causal, key_lens, scale, st);
+    return launch_fwd_tc<128>(q, k, v, o, lse, B, Hq, Hkv, T, S, causal, key_lens, scale, st);
+  }
+  if (dtype == ATTN_F32) {
+    if (D > 256) return ATTN_ERR_UNSUPPORTED;
+    if (!aligned4(q) || !aligned4(k) || !aligned4(v) || !aligned4(o)) return ATTN_ERR_INVALID_ARG;
+    const int nc = (D + 31) / 32;
+#define ATTN_F32_CASE(N) \
+  case N: return launch_fwd_f32<N>(q, k, v, o, lse, B, Hq, Hkv, T, S, D, causal, key_lens, scale, st);
+    switch (nc) {
+      ATTN_F32_CASE(1) ATTN_F32_CASE(2) ATTN_F32_CASE(3) ATTN_F32_CASE(4)
+      ATTN_F32_CASE(5) ATTN_F32_CASE(6) ATTN_F32_CASE(7) ATTN_F32_CASE(8)
+      default: return ATTN_ERR_UNSUPPORTED;
+    }
+#undef ATTN_F32_CASE
+  }
+  return ATTN_ERR_INVALID_ARG;
+}
+
+size_t attn_decode_workspace_size(int B, int Hq, int S_max, int D) {
+  if (B <= 0 || Hq <= 0 || S_max <= 0 || D <= 0) return 0;
+  return (size_t)B * Hq * attn::decode::max_splits(S_max) * ((size_t)D + 2) * sizeof(float);
+}
+
+int attn_decode(const void* q, const void* kcache, const void* vcache, const int32_t* kv_lens,
+                void* o, float* lse, int B, int Hq, int Hkv, int S_max, int D, int dtype,
+                float scale, void* workspace, size_t ws_bytes, attn_stream_t stream) {
+  if (!q || !kcache || !vcache || !kv_lens || !o) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || S_max <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !finite_positive(scale)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  const int G = Hq / Hkv;
+  if (G > 16 || (G & (G - 1)) != 0) return ATTN_ERR_UNSUPPORTED;
+  if (B > 65535 || Hkv > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
+      !aligned4(kv_lens) || (lse != nullptr && !aligned4(lse)))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_decode_workspace_size(B, Hq, S_max, D);
+  if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+
+  attn::decode::Params p;
+  p.q = q;
+  p.kc = kcache;
+  p.vc = vcache;
+  p.kv_lens = kv_lens;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.S_max = S_max;
+  p.splits = attn::decode::max_splits(S_max);
+  const size_t slots = (size_t)B * Hq * p.splits;
+  p.ws_o = static_cast<float*>(workspace);
+  p.ws_m = p.ws_o + slots * D;
+  p.ws_l = p.ws_m + slots;
+  p.scale_log2 = scale * kLog2e;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == ATTN_BF16) {
+    return D == 64 ? launch_decode_d<__nv_bfloat16, 64>(p, G, st)
+                   : launch_decode_d<__nv_bfloat16, 128>(p, G, st);
+  }
+  return D == 64 ? launch_decode_d<float, 64>(p, G, st) : launch_decode_d<float, 128>(p, G, st);
+}
+
+int kv_cache_append(void* kcache, void* vcache, const void* k_new, const void* v_new,
+                    const int32_t* pos, int B, int Hkv, int S_max, int D, int dtype,
+                    int* dev_status, attn_stream_t stream) {
+  if (!kcache || !vcache || !k_new || !v_new || !pos) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hkv <= 0 || S_max <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  size_t esz;
+  if (dtype == ATTN_BF16) esz = 2;
+  else if (dtype == ATTN_F32) esz = 4;
+  else return ATTN_ERR_INVALID_ARG;
+  const size_t row_bytes = (size_t)D * esz;
+  if (row_bytes % 16 != 0) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(kcache) || !aligned16(vcache) || !aligned16(k_new) || !aligned16(v_new) ||
+      !aligned4(pos) || (dev_status != nullptr && !aligned4(dev_status)))
+    return ATTN_ERR_INVALID_ARG;
+  const int vec_per_row = (int)(row_bytes / 16);
+  const long long total = (long long)B * Hkv * vec_per_row;
+  const int threads = 256;
+  long long blocks = (total + threads - 1) / threads;
+  if (blocks > 148 * 16) blocks = 148 * 16;
+  attn::kv_append_kernel<<<(unsigned)blocks, threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4*>(kcache), static_cast<uint4*>(vcache), static_cast<const uint4*>(k_new),
+      static_cast<const uint4*>(v_new), pos, B, Hkv, S_max, vec_per_row, dev_status);
+  return launch_status();
+}
+
+const char* attn_status_string(int status) {
+  switch (status) {
+    case ATTN_OK: return "ATTN_OK: success";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG: invalid argument";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: unsupported shape or type";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: decode workspace missing or too small";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: CUDA error at launch";
+    default: return "unknown attn status";
+  }
+}
+
+unsigned long long attn_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int attn_device_error(int* code, int clear) {
+  int v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, attn::g_attn_error, sizeof(int)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (code != nullptr) *code = v;
+  if (clear) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(attn::g_attn_error, &zero, sizeof(int)) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+}  // extern "C"

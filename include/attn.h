@@ -1,0 +1,190 @@
+/*
+ * attn.h -- C ABI of libattn.so: exact scaled-dot-product attention on B300
+ * (sm_103a), computed tile by tile with an online softmax so that the T x S
+ * score matrix never reaches device memory.
+ *
+ *   O = softmax(Q K^T * scale + mask) V
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - All tensor arguments are DEVICE pointers to contiguous row-major arrays
+ *    that the caller allocates, owns and frees.  The library keeps no
+ *    per-call state and allocates no device memory on these paths.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  A non-zero return means nothing was launched, except
+ *    ATTN_ERR_CUDA, which reports a launch error seen right after launching.
+ *  - Element types: ATTN_BF16 inputs/outputs with float32 softmax and
+ *    accumulation, or ATTN_F32 end to end (no TF32).  LSE is always float32.
+ *  - Layouts ("Implementing attention from scratch", Core ideas, Shapes first):
+ *      q, o     [B, Hq, T, D]
+ *      k, v     [B, Hkv, S, D]
+ *      lse      [B, Hq, T]
+ *    Grouped-query attention ("Self-Attention: Implementation, Complexity,
+ *    and Efficient Variants", follow-up on MQA/GQA; "Implementing attention
+ *    from scratch", KV caching): Hq must be a multiple of Hkv, and query head
+ *    h reads KV head h / (Hq / Hkv) (contiguous groups).
+ *  - Masks ("Implementing attention from scratch", Masks and KV caching;
+ *    "Building a causal self-attention block from scratch in PyTorch",
+ *    Step 2): query row i sits at key position p_i = i + S - T (bottom-right
+ *    alignment).  With L = key_lens[b] (S when key_lens is NULL):
+ *        row i is a padded row       iff p_i >= L
+ *        key j is visible to row i   iff j < L and (!causal or j <= p_i)
+ *    A padded row, or a row that sees no key, is defined as O = 0 and
+ *    LSE = -inf (the pages note a fully masked softmax row is NaN and must
+ *    be handled explicitly).
+ *  - LSE[i] = ln(sum over visible j of exp(scale * q_i . k_j)).
+ */
+#ifndef ATTN_B300_ATTN_H_
+#define ATTN_B300_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA
+ * include. */
+typedef struct CUstream_st* attn_stream_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, ...     */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement  */
+  ATTN_ERR_WORKSPACE = 3,   /* decode workspace missing or too small        */
+  ATTN_ERR_CUDA = 4         /* CUDA runtime/driver error at or before launch */
+} attn_status;
+
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
+
+/*
+ * attn_fwd -- prefill forward: O and (optionally) the per-row LSE.
+ *
+ * Computes the masked attention described above for every (b, h, i)
+ * ("Implementing attention from scratch", Core ideas: Shapes first, Masks,
+ * Stable softmax; "FlashAttention", Transformers in Action section 9.4.1,
+ * Figure 9.8: Q and K/V tiles stream through on-chip memory, partial results
+ * are rescaled as the running row maximum grows, and the n x m score matrix
+ * is never materialised).
+ *
+ *   q        [B,Hq,T,D]  dtype          (read)
+ *   k, v     [B,Hkv,S,D] dtype          (read)
+ *   o        [B,Hq,T,D]  dtype          (written; padded rows written as 0)
+ *   lse      [B,Hq,T]    float32        (written; NULL = do not emit)
+ *   key_lens [B]         int32, device  (read; NULL = every key valid;
+ *                                        each value must lie in [0, S] --
+ *                                        values are read on the device and
+ *                                        clamped to [0, S])
+ *   causal   0 or 1
+ *   scale    > 0, finite (typically 1/sqrt(D))
+ *
+ * Supported: B, Hq, Hkv, T, S >= 1, Hq % Hkv == 0.
+ *   ATTN_BF16: D in {64, 128}; q, k, v, o 16-byte aligned.  Tensor-core
+ *              path (tcgen05 MMAs with TMEM accumulators, TMA tile loads).
+ *   ATTN_F32:  1 <= D <= 256; 4-byte aligned.  Exact float32 path on the
+ *              CUDA cores (FFMA, accurate expf), no TF32.
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED or
+ * ATTN_ERR_CUDA.
+ */
+ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int Hq, int Hkv, int T, int S, int D, int dtype,
+             int causal, const int32_t* key_lens, float scale,
+             attn_stream_t stream);
+
+/*
+ * attn_decode_workspace_size -- bytes of device scratch attn_decode needs for
+ * a batch of B sequences, Hq query heads, caches of S_max positions and head
+ * size D.  The caller allocates it (any alignment >= 16 bytes) and may reuse
+ * it across calls on the same stream.  Returns 0 for invalid sizes.
+ */
+ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int S_max, int D);
+
+/*
+ * attn_decode -- one decode step: a single new query per (b, h) attends over
+ * the first kv_lens[b] cache rows ("Implementing attention from scratch",
+ * KV caching: a decode step attends one new query over the cached
+ * positions; with the query at position kv_lens[b]-1 the bottom-right causal
+ * mask admits exactly rows 0..kv_lens[b]-1).  Split-KV: chunks of the cache
+ * are reduced independently to (partial O, running max, denominator) and a
+ * second pass merges them with the same exp(m_old - m_new) rescaling the
+ * online softmax uses ("Implementing attention from scratch", Stable
+ * softmax).
+ *
+ *   q         [B,Hq,D]          dtype   (read)
+ *   kcache    [B,Hkv,S_max,D]   dtype   (read; rows >= kv_lens[b] ignored)
+ *   vcache    [B,Hkv,S_max,D]   dtype   (read)
+ *   kv_lens   [B] int32, device         (read; keys per sequence, INCLUDING
+ *                                        the token just appended; values are
+ *                                        clamped to [0, S_max]; 0 gives O = 0,
+ *                                        LSE = -inf)
+ *   o         [B,Hq,D]          dtype   (written)
+ *   lse       [B,Hq] float32            (written; NULL = do not emit)
+ *   workspace device scratch of >= attn_decode_workspace_size(B,Hq,S_max,D)
+ *             bytes, 16-byte aligned; contents need no initialisation.
+ *
+ * Supported: dtype ATTN_BF16 or ATTN_F32; D in {64, 128}; Hq % Hkv == 0 and
+ * Hq / Hkv <= 16; q, caches, o 16-byte aligned.
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
+ * ATTN_ERR_WORKSPACE or ATTN_ERR_CUDA.
+ */
+ATTN_API int attn_decode(const void* q, const void* kcache, const void* vcache,
+                const int32_t* kv_lens, void* o, float* lse, int B, int Hq,
+                int Hkv, int S_max, int D, int dtype, float scale,
+                void* workspace, size_t ws_bytes, attn_stream_t stream);
+
+/*
+ * kv_cache_append -- write one new token's K and V rows per (b, kv head) at
+ * cache position pos[b] ("Building a causal self-attention block from
+ * scratch in PyTorch", Step 5, KVCache.update appends the new token along
+ * the sequence axis; "Implementing attention from scratch", KV caching: the
+ * new token's offset is the cache length).  The cache is preallocated to
+ * S_max positions, so an append is an O(1) row copy, not a concatenation.
+ *
+ *   kcache, vcache  [B,Hkv,S_max,D] dtype  (row pos[b] written)
+ *   k_new, v_new    [B,Hkv,D]       dtype  (read)
+ *   pos             [B] int32, device      (read, not modified: pass the
+ *                                           cache length before the append,
+ *                                           then decode with kv_lens = pos+1)
+ *   dev_status      int32, device, or NULL (for every (b, g) whose pos[b] is
+ *                                           outside [0, S_max) the row is
+ *                                           NOT written and bit 0 is OR-ed
+ *                                           into *dev_status)
+ *
+ * Supported: dtype ATTN_BF16 or ATTN_F32; D >= 1 with D * element size a
+ * multiple of 16 bytes; all tensor pointers 16-byte aligned.
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG or ATTN_ERR_CUDA.
+ */
+ATTN_API int kv_cache_append(void* kcache, void* vcache, const void* k_new,
+                    const void* v_new, const int32_t* pos, int B, int Hkv,
+                    int S_max, int D, int dtype, int* dev_status,
+                    attn_stream_t stream);
+
+/* attn_status_string -- static, human-readable text for a status code. */
+ATTN_API const char* attn_status_string(int status);
+
+/*
+ * Diagnostics (not part of the attention arithmetic).
+ *
+ * attn_kernel_launches -- number of kernels this library has launched in
+ *   this process (all entry points, all devices).  Host-side counter.
+ *
+ * attn_device_error -- reads (and, if `clear`, resets) the current device's
+ *   error word, which a kernel sets instead of trapping when an internal
+ *   pipeline wait exceeds its time limit.  0 means no error.  Synchronises
+ *   the device.  Returns ATTN_OK or ATTN_ERR_CUDA.
+ */
+ATTN_API unsigned long long attn_kernel_launches(void);
+ATTN_API int attn_device_error(int* code, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_B300_ATTN_H_ */

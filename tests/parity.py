@@ -1,0 +1,62 @@
+"""Helpers for the GPU-vs-oracle parity tests.
+
+Tolerances (float64 oracle as reference, same input values on both sides):
+  float32 path: O max abs <= 2e-5, LSE max abs <= 1e-4
+  bf16 path:    O max abs <= 1.5e-2 and mean abs <= 2e-3, LSE max abs <= 2e-3
+Rows with no visible key (padded rows included) must be exactly O = 0 and
+LSE = -inf on the GPU; they are excluded from the tolerance statistics.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from workloads import to_numpy_exact
+
+TOL = {
+    torch.float32: {"max": 2e-5, "mean": 2e-5, "lse": 1e-4},
+    torch.bfloat16: {"max": 1.5e-2, "mean": 2e-3, "lse": 2e-3},
+}
+
+
+def oracle_fwd(q, k, v, causal, key_lens, scale, rows=None):
+    qn, bf = to_numpy_exact(q)
+    kn, _ = to_numpy_exact(k)
+    vn, _ = to_numpy_exact(v)
+    kl = None if key_lens is None else key_lens.cpu().numpy()
+    return oracle.attn_fwd(qn, kn, vn, causal=causal, key_lens=kl, scale=scale,
+                           bf16=bf, rows=rows)
+
+
+def oracle_decode(q, kc, vc, kv_lens, scale):
+    qn, bf = to_numpy_exact(q)
+    kn, _ = to_numpy_exact(kc)
+    vn, _ = to_numpy_exact(vc)
+    return oracle.attn_decode(qn, kn, vn, kv_lens.cpu().numpy(), scale=scale, bf16=bf)
+
+
+def compare(o_gpu: torch.Tensor, lse_gpu, o_ref: np.ndarray, lse_ref: np.ndarray,
+            dtype, what=""):
+    """Element-by-element comparison; returns the error statistics."""
+    tol = TOL[dtype]
+    og = o_gpu.detach().double().cpu().numpy().reshape(o_ref.shape)
+    empty = ~np.isfinite(lse_ref)
+    # Rows with no visible key: exact zeros (and -inf LSE) required.
+    assert np.all(og[empty] == 0.0), f"{what}: rows without visible keys must be exactly 0"
+    good = ~empty
+    assert np.isfinite(og).all(), f"{what}: non-finite outputs"
+    err = np.abs(og[good] - o_ref[good]) if good.any() else np.zeros(1)
+    stats = {"max": float(err.max()), "mean": float(err.mean()), "rows": int(good.sum()),
+             "empty_rows": int(empty.sum())}
+    assert stats["max"] <= tol["max"], f"{what}: max abs err {stats['max']:.3g} > {tol['max']}"
+    assert stats["mean"] <= tol["mean"], f"{what}: mean abs err {stats['mean']:.3g} > {tol['mean']}"
+    if lse_gpu is not None:
+        lg = lse_gpu.detach().double().cpu().numpy().reshape(lse_ref.shape)
+        assert np.all(lg[empty] == -np.inf), f"{what}: LSE of empty rows must be -inf"
+        if good.any():
+            le = np.abs(lg[good] - lse_ref[good])
+            stats["lse_max"] = float(le.max())
+            assert stats["lse_max"] <= tol["lse"], \
+                f"{what}: LSE max abs err {stats['lse_max']:.3g} > {tol['lse']}"
+    return stats

@@ -1,0 +1,121 @@
+"""The C-ABI library loads and exports what include/attn.h declares (CPU).
+
+No kernel is launched here: every call below is rejected by host-side
+validation before any CUDA runtime call, or is a pure host function.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_tiled_attention_49_b300 import build
+    build.build()
+    import exact_tiled_attention_49_b300 as m
+    return m.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["attn_fwd", "attn_decode", "attn_decode_workspace_size", "kv_cache_append",
+              "attn_status_string"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_binding_covers_header():
+    import exact_tiled_attention_49_b300 as m
+    assert sorted(m.SIGNATURES) == declared_functions()
+
+
+def test_only_declared_symbols_exported():
+    from exact_tiled_attention_49_b300 import LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines()
+                if line.split() and line.split()[-2] in ("T", "W")}
+    ours = {s for s in exported if s.startswith(("attn_", "kv_cache"))}
+    assert ours == set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        s = lib.attn_status_string(code).decode()
+        assert s.startswith("ATTN_")
+    assert "unknown" in lib.attn_status_string(99).decode()
+
+
+def test_workspace_size_formula(lib):
+    # partial O (D floats) + running max + denominator per (b, h, 256-key chunk)
+    assert lib.attn_decode_workspace_size(64, 32, 8193, 128) == 64 * 32 * 33 * 130 * 4
+    assert lib.attn_decode_workspace_size(1, 1, 256, 64) == 1 * 1 * 1 * 66 * 4
+    assert lib.attn_decode_workspace_size(0, 1, 1, 64) == 0
+
+
+FAKE = ctypes.c_void_p(0x10000)  # 16-byte aligned, never dereferenced
+MIS = ctypes.c_void_p(0x10002)   # misaligned
+
+
+def _fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None, B=1, Hq=1, Hkv=1, T=8, S=8, D=64,
+         dt=1, causal=0, lens=None, scale=0.125):
+    return lib.attn_fwd(q, k, v, o, lse, B, Hq, Hkv, T, S, D, dt, causal, lens, scale, None)
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    assert _fwd(lib, q=None) == 1
+    assert _fwd(lib, B=0) == 1
+    assert _fwd(lib, T=-1) == 1
+    assert _fwd(lib, Hq=3, Hkv=2) == 1
+    assert _fwd(lib, scale=0.0) == 1
+    assert _fwd(lib, scale=float("nan")) == 1
+    assert _fwd(lib, D=96) == 2            # bf16 supports D in {64, 128}
+    assert _fwd(lib, D=300, dt=0) == 2     # fp32 supports D <= 256
+    assert _fwd(lib, q=MIS) == 1           # TMA needs 16-byte alignment
+    assert _fwd(lib, dt=7) == 1
+
+
+def test_decode_rejects_bad_arguments(lib):
+    ws = lib.attn_decode_workspace_size(2, 4, 100, 64)
+
+    def dec(kv_lens=FAKE, D=64, Hq=4, Hkv=2, ws_ptr=FAKE, ws_bytes=ws, dt=1):
+        return lib.attn_decode(FAKE, FAKE, FAKE, kv_lens, FAKE, None, 2, Hq, Hkv, 100, D, dt,
+                               0.125, ws_ptr, ws_bytes, None)
+    assert dec(kv_lens=None) == 1
+    assert dec(Hq=6, Hkv=4) == 1
+    assert dec(D=96) == 2
+    assert dec(Hq=64, Hkv=2) == 2          # group of 32 query heads per KV head
+    assert dec(ws_ptr=None) == 3
+    assert dec(ws_bytes=ws - 4) == 3
+
+
+def test_append_rejects_bad_arguments(lib):
+    def app(D=64, dt=1, pos=FAKE, k=FAKE):
+        return lib.kv_cache_append(k, FAKE, FAKE, FAKE, pos, 2, 2, 10, D, dt, None, None)
+    assert app(pos=None) == 1
+    assert app(D=4) == 1                   # 8-byte rows cannot be copied as 16-byte vectors
+    assert app(k=MIS) == 1
+    assert app(dt=5) == 1
+
+
+def test_launch_counter_is_host_side(lib):
+    assert isinstance(lib.attn_kernel_launches(), int)
