@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);
     }
     const bool has = ok && row_ok && (l > 0.f);
-    const float inv = 1.f / l;
+    const float inv = has ? 1.f / l : 0.f;
     __nv_bfloat16* orow =
         reinterpret_cast<__nv_bfloat16*>(p.o) + ((((size_t)b * p.Hq + h) * p.T) + i) * D;
     if (__any_sync(0xffffffffu, has)) {

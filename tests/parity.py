@@ -36,9 +36,20 @@ def oracle_decode(q, kc, vc, kv_lens, scale):
     return oracle.attn_decode(qn, kn, vn, kv_lens.cpu().numpy(), scale=scale, bf16=bf)
 
 
+def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
+    """Half the spacing of bfloat16 numbers at |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(x), np.finfo(np.float32).tiny)
+    return np.ldexp(1.0, np.floor(np.log2(ax)).astype(np.int64) - 8)
+
+
 def compare(o_gpu: torch.Tensor, lse_gpu, o_ref: np.ndarray, lse_ref: np.ndarray,
-            dtype, what=""):
-    """Element-by-element comparison; returns the error statistics."""
+            dtype, what="", out_rounding=False):
+    """Element-by-element comparison; returns the error statistics.
+
+    ``out_rounding`` widens the per-element max bound by half a bf16 ulp of
+    the exact value: only for stress cases whose outputs exceed magnitude 2,
+    where storing O in bf16 alone can cost up to 1.56e-2.
+    """
     tol = TOL[dtype]
     og = o_gpu.detach().double().cpu().numpy().reshape(o_ref.shape)
     empty = ~np.isfinite(lse_ref)
@@ -49,7 +60,12 @@ def compare(o_gpu: torch.Tensor, lse_gpu, o_ref: np.ndarray, lse_ref: np.ndarray
     err = np.abs(og[good] - o_ref[good]) if good.any() else np.zeros(1)
     stats = {"max": float(err.max()), "mean": float(err.mean()), "rows": int(good.sum()),
              "empty_rows": int(empty.sum())}
-    assert stats["max"] <= tol["max"], f"{what}: max abs err {stats['max']:.3g} > {tol['max']}"
+    if out_rounding and good.any():
+        excess = err - bf16_half_ulp(o_ref[good])
+        assert excess.max() <= tol["max"], \
+            f"{what}: max abs err beyond output rounding {excess.max():.3g} > {tol['max']}"
+    else:
+        assert stats["max"] <= tol["max"], f"{what}: max abs err {stats['max']:.3g} > {tol['max']}"
     assert stats["mean"] <= tol["mean"], f"{what}: mean abs err {stats['mean']:.3g} > {tol['mean']}"
     if lse_gpu is not None:
         lg = lse_gpu.detach().double().cpu().numpy().reshape(lse_ref.shape)

@@ -26,7 +26,7 @@ def E():
     return m
 
 
-def _run(E, B, Hq, Hkv, T, S, D, causal, lens, seed=1, q_scale=1.0):
+def _run(E, B, Hq, Hkv, T, S, D, causal, lens, seed=1, q_scale=1.0, out_rounding=False):
     x = workloads.prefill_inputs(B, Hq, Hkv, T, S, D, "bf16", seed=seed, device="cuda",
                                  lens=lens, q_scale=q_scale)
     scale = 1.0 / math.sqrt(D)
@@ -34,7 +34,8 @@ def _run(E, B, Hq, Hkv, T, S, D, causal, lens, seed=1, q_scale=1.0):
                         scale=scale)
     torch.cuda.synchronize()
     ro, rl = oracle_fwd(x["q"], x["k"], x["v"], causal, x["key_lens"], scale)
-    st = compare(o, lse, ro, rl, torch.bfloat16, f"bf16 {(B, Hq, Hkv, T, S, D, causal, lens)}")
+    st = compare(o, lse, ro, rl, torch.bfloat16, f"bf16 {(B, Hq, Hkv, T, S, D, causal, lens)}",
+                 out_rounding=out_rounding)
     assert E.attn_device_error(clear=True) == 0
     return st
 
@@ -68,8 +69,11 @@ def test_prefill_bf16(E, case):
 @pytest.mark.parametrize("q_scale", [2.0, 8.0])
 def test_large_scores_rescale(E, q_scale):
     """Larger query scale makes the running maximum move often, exercising
-    the lazy O rescale."""
-    _run(E, 1, 4, 4, 384, 384, 128, True, None, seed=9, q_scale=q_scale)
+    the lazy O rescale.  With Q x 8 the softmax is nearly one-hot and |O|
+    exceeds 2, where storing O in bf16 alone can cost 1.56e-2, so that case
+    allows half a bf16 ulp of the exact value on top of the tolerance."""
+    _run(E, 1, 4, 4, 384, 384, 128, True, None, seed=9, q_scale=q_scale,
+         out_rounding=q_scale > 4)
 
 
 def test_output_buffer_and_no_lse(E):
