@@ -10,13 +10,15 @@ ABI (``include/attn.h``); this package is a thin ctypes binding of it.
 """
 from ._lib import (ATTN_BF16, ATTN_ERR_CUDA, ATTN_ERR_INVALID_ARG,  # noqa: F401
                    ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_F32, ATTN_OK,
-                   LIB_PATH, SIGNATURES, AttnError, attn_decode,
+                   LIB_PATH, NOALLOC_SCRATCH_BYTES, SIGNATURES, AttnError, attn_decode,
+                   attn_decode_noalloc,
                    attn_decode_workspace_size, attn_device_error, attn_fwd,
                    attn_kernel_launches, attn_status_string, kv_cache_append, load,
                    status_string)
 
 __all__ = [
-    "attn_fwd", "attn_decode", "attn_decode_workspace_size", "kv_cache_append",
+    "attn_fwd", "attn_decode", "attn_decode_workspace_size", "attn_decode_noalloc",
+    "kv_cache_append",
     "attn_status_string", "attn_kernel_launches", "attn_device_error", "AttnError",
     "load", "LIB_PATH",
 ]

@@ -26,6 +26,7 @@ SIGNATURES = {
     "attn_decode_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
                          ctypes.c_size_t, _P]),
+    "attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "kv_cache_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_kernel_launches": (ctypes.c_ulonglong, []),
@@ -177,6 +178,35 @@ def attn_decode(q, kcache, vcache, kv_lens, o=None, lse=None, workspace=None,
                          float(scale), _dev(workspace, "workspace"),
                          workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "attn_decode")
+    return o, lse
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20  # ATTN_NOALLOC_SCRATCH_BYTES in include/attn.h
+
+
+def attn_decode_noalloc(q, kcache, vcache, kv_lens, o, lse=None, scale=None, stream=None):
+    """Decode step that allocates nothing: for callers that cannot allocate
+    device memory (a host framework that owns all of it, or a real-time loop
+    that cannot afford cudaMalloc's synchronisation).  The outputs `o` (like
+    q) and optional `lse` (float32 [B,Hq]) must be given; the library's fixed
+    16 MiB device scratch array replaces the workspace.  Calls share that
+    array, so calls that may overlap on the GPU must be serialised."""
+    lib = load()
+    B, Hq, D = q.shape
+    Bk, Hkv, S_max, Dk = kcache.shape
+    if Bk != B or Dk != D or tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError("q/cache shape mismatch")
+    if tuple(o.shape) != tuple(q.shape):
+        raise ValueError("o must have q's shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lp = _dev(lse, "lse", dtype=torch.float32) if lse is not None else None
+    rc = lib.attn_decode_noalloc(_dev(q, "q", ndim=3), _dev(kcache, "kcache", ndim=4),
+                                 _dev(vcache, "vcache", ndim=4),
+                                 _dev(kv_lens, "kv_lens", dtype=torch.int32, ndim=1),
+                                 _dev(o, "o", dtype=q.dtype, ndim=3), lp, B, Hq, Hkv, S_max, D,
+                                 _dtype_code(q), float(scale), _stream(stream))
+    _check(rc, "attn_decode_noalloc")
     return o, lse
 
 

@@ -259,6 +259,52 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, const int
   return D == 64 ? launch_decode_d<float, 64>(p, G, st) : launch_decode_d<float, 128>(p, G, st);
 }
 
+}  // extern "C"
+
+// ------------------------------------------------ decode without allocation
+//
+// Scratch for attn_decode_noalloc: a fixed device array defined here, so a
+// caller that cannot allocate device memory still gets a decode workspace.
+// Host code must not pass `g_noalloc_scratch` itself to a kernel (on the host
+// that name is only a stand-in); its device address is looked up once per
+// device with cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device (first call per
+// device does the lookup); nullptr on failure.
+void* noalloc_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_decode_noalloc(const void* q, const void* kcache, const void* vcache,
+                        const int32_t* kv_lens, void* o, float* lse, int B, int Hq, int Hkv,
+                        int S_max, int D, int dtype, float scale, attn_stream_t stream) {
+  const size_t need = attn_decode_workspace_size(B, Hq, S_max, D);
+  if (need == 0) return ATTN_ERR_INVALID_ARG;
+  if (need > ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_WORKSPACE;
+  void* scratch = noalloc_scratch();
+  if (scratch == nullptr) return ATTN_ERR_CUDA;
+  return attn_decode(q, kcache, vcache, kv_lens, o, lse, B, Hq, Hkv, S_max, D, dtype, scale,
+                     scratch, ATTN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 int kv_cache_append(void* kcache, void* vcache, const void* k_new, const void* v_new,
                     const int32_t* pos, int B, int Hkv, int S_max, int D, int dtype,
                     int* dev_status, attn_stream_t stream) {

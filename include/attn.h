@@ -140,6 +140,38 @@ ATTN_API int attn_decode(const void* q, const void* kcache, const void* vcache,
                 void* workspace, size_t ws_bytes, attn_stream_t stream);
 
 /*
+ * attn_decode_noalloc -- attn_decode for callers that cannot allocate device
+ * memory.  (The pages have no counterpart; this is a library convenience.)
+ *
+ * Some callers cannot call cudaMalloc or hand the library a buffer: plugins
+ * whose host framework owns every byte of device memory through its own
+ * allocator, or real-time loops where cudaMalloc's implicit device
+ * synchronisation and unbounded latency are not acceptable.  This entry
+ * point takes the same arguments as attn_decode minus the workspace, and
+ * uses instead a scratch array of ATTN_NOALLOC_SCRATCH_BYTES that the
+ * library defines at file scope in device memory.  Every GPU on which the
+ * library is loaded holds that array until the process exits.
+ *
+ *  - It allocates nothing and calls no allocating routine.
+ *  - Requests whose workspace would exceed ATTN_NOALLOC_SCRATCH_BYTES
+ *    (see attn_decode_workspace_size) return ATTN_ERR_WORKSPACE without
+ *    launching anything; use attn_decode with your own workspace then.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls share the one array, which keeps whatever the last call left
+ *    there.  Nothing in it needs clearing: each call writes every scratch
+ *    slot it reads.  Calls that can overlap on the GPU (different streams,
+ *    or different host threads) race on the array and must be serialised by
+ *    the caller.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+ATTN_API int attn_decode_noalloc(const void* q, const void* kcache, const void* vcache,
+                                 const int32_t* kv_lens, void* o, float* lse, int B,
+                                 int Hq, int Hkv, int S_max, int D, int dtype,
+                                 float scale, attn_stream_t stream);
+
+/*
  * kv_cache_append -- write one new token's K and V rows per (b, kv head) at
  * cache position pos[b] ("Building a causal self-attention block from
  * scratch in PyTorch", Step 5, KVCache.update appends the new token along
