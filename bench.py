@@ -248,33 +248,54 @@ def build_case(wid, device):
     return case
 
 
-def run_step(E, c, ev=None):
-    """One step.  `ev` (optional) maps kernel group -> (start, end) events."""
+def step_groups(c):
+    """Kernel groups of one step, in order: (name, callable issuing them)."""
+    import exact_tiled_attention_49_b300 as E
     w = c["w"]
     scale = 1.0 / math.sqrt(w.D)
-
-    def rec(name, i):
-        if ev is not None and name in ev:
-            ev[name][i].record()
-
+    groups = []
     if w.kind == "prefill":
-        rec("prefill", 0)
-        E.attn_fwd(c["q"], c["k"], c["v"], o=c["o"], lse=c["lse"], causal=w.causal,
-                   key_lens=c["key_lens"], scale=scale)
-        rec("prefill", 1)
+        groups.append(("prefill", lambda: E.attn_fwd(
+            c["q"], c["k"], c["v"], o=c["o"], lse=c["lse"], causal=w.causal,
+            key_lens=c["key_lens"], scale=scale)))
         if "dec" in c:
             d = c["dec"]
-            rec("decode", 0)
-            E.kv_cache_append(d["kcache"], d["vcache"], d["k_new"], d["v_new"], d["pos"])
-            E.attn_decode(d["q"], d["kcache"], d["vcache"], d["kv_len"], o=d["o"], lse=d["lse"],
-                          workspace=d["ws"], scale=scale)
-            rec("decode", 1)
+
+            def dec():
+                E.kv_cache_append(d["kcache"], d["vcache"], d["k_new"], d["v_new"], d["pos"])
+                E.attn_decode(d["q"], d["kcache"], d["vcache"], d["kv_len"], o=d["o"],
+                              lse=d["lse"], workspace=d["ws"], scale=scale)
+            groups.append(("decode", dec))
     else:
-        rec("decode", 0)
-        E.kv_cache_append(c["kcache"], c["vcache"], c["k_new"], c["v_new"], c["cache_len"])
-        E.attn_decode(c["q"], c["kcache"], c["vcache"], c["kv_len"], o=c["o"], lse=c["lse"],
-                      workspace=c["ws"], scale=scale)
-        rec("decode", 1)
+        def dec():
+            E.kv_cache_append(c["kcache"], c["vcache"], c["k_new"], c["v_new"], c["cache_len"])
+            E.attn_decode(c["q"], c["kcache"], c["vcache"], c["kv_len"], o=c["o"], lse=c["lse"],
+                          workspace=c["ws"], scale=scale)
+        groups.append(("decode", dec))
+    return groups
+
+
+def run_step(E, c):
+    """One step issued call by call through the public API."""
+    for _, fn in step_groups(c):
+        fn()
+
+
+def capture_graphs(E, c):
+    """One CUDA graph per kernel group of the step, captured once and replayed
+    in the timed region so that microsecond kernels are not separated by
+    host-side launch latency.  Returns [(name, graph)] and the number of
+    library kernels one step launches."""
+    import torch
+    graphs = []
+    n0 = E.attn_kernel_launches()
+    for name, fn in step_groups(c):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs.append((name, g))
+    torch.cuda.synchronize()
+    return graphs, E.attn_kernel_launches() - n0
 
 
 def run_e2e(E, c, steps, device):
@@ -404,27 +425,33 @@ def bench_ours(args):
     if E.attn_device_error(clear=True) != 0:
         raise RuntimeError("device error during warm-up")
 
-    groups = ["prefill", "decode"] if "dec" in c else (["prefill"] if w.kind == "prefill" else ["decode"])
+    graphs, launches_per_step = capture_graphs(E, c)
+    for _ in range(2):                        # warm replays of the captured step
+        flush.zero_()
+        for _, g in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+    groups = [name for name, _ in graphs]
     K = args.steps
-    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(K)]
-    ev_k = [{g: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for g in groups} for _ in range(K)]
-    launches0 = E.attn_kernel_launches()
+    # events[s] = [start, end of group 0, end of group 1, ...]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
+              for _ in range(K)]
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(device) as clk:
         for s in range(K):
             flush.zero_()                     # L2 flush, outside the timed events
-            ev_step[s][0].record()
-            run_step(E, c, ev_k[s])
-            ev_step[s][1].record()
+            events[s][0].record()
+            for i, (_, g) in enumerate(graphs):
+                g.replay()
+                events[s][i + 1].record()
         torch.cuda.synchronize()
     barrier(ws)
-    launches = E.attn_kernel_launches() - launches0
-    step_ms = [a.elapsed_time(b) for a, b in ev_step]
+    launches = launches_per_step * K
+    step_ms = [ev[0].elapsed_time(ev[-1]) for ev in events]
     total_ms = reduce_max(sum(step_ms), ws, device)
-    kern_ms = {g: sum(e[g][0].elapsed_time(e[g][1]) for e in ev_k) / K for g in groups}
+    kern_ms = {g: sum(ev[i].elapsed_time(ev[i + 1]) for ev in events) / K
+               for i, g in enumerate(groups)}
     if E.attn_device_error(clear=True) != 0:
         raise RuntimeError("device error during the timed region")
 
@@ -465,6 +492,7 @@ def bench_ours(args):
                            "peak_source": peaks["source"] + " HBM copy"}
     cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
            "l2": "flushed between steps (256 MiB write, outside the timed events)",
+           "timing": "CUDA events around CUDA-graph replays of each kernel group of the step",
            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
            "algorithmic_work_per_step": c["flops"] if w.kind == "prefill" else c["dec_bytes"]}
     if w.kind == "prefill":

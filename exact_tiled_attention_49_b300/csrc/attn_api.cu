@@ -74,6 +74,11 @@ bool ensure_smem(K kernel, size_t bytes, std::atomic<uint64_t>& done_mask) {
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
       cudaSuccess)
     return false;
+  // Ask for the largest shared-memory carveout so that as many CTAs as the
+  // shared-memory budget allows can be resident on one SM.
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+    return false;
   done_mask.fetch_or(bit, std::memory_order_acq_rel);
   return true;
 }
