@@ -6,11 +6,14 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
+#include <utility>
 
 #include "../../include/attn.h"
 #include "append.cuh"
@@ -64,6 +67,21 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, int D, int rows, long long
   return r == CUDA_SUCCESS;
 }
 
+// 2-D bf16 tensor [rows, D] (D contiguous) loaded as boxes of 64 columns x
+// `box_rows` rows with 128-byte swizzle.
+bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, int D, long long rows, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Opt a kernel into more than 48 KB of dynamic shared memory, once per device.
 template <typename K>
 bool ensure_smem(K kernel, size_t bytes, std::atomic<uint64_t>& done_mask) {
@@ -81,6 +99,38 @@ bool ensure_smem(K kernel, size_t bytes, std::atomic<uint64_t>& done_mask) {
     return false;
   done_mask.fetch_or(bit, std::memory_order_acq_rel);
   return true;
+}
+
+// Streaming-multiprocessor count of the current device (cached per device).
+int num_sms() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  int v = cache[dev].load(std::memory_order_relaxed);
+  if (v > 0) return v;
+  if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+    v = 148;
+  cache[dev].store(v, std::memory_order_relaxed);
+  return v;
+}
+
+// Launch as a programmatic dependent of the previous kernel in the stream: the
+// kernel's CTAs may be scheduled while that kernel drains and wait in
+// hardware (griddepcontrol.wait) before touching its results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 int launch_status() {
@@ -154,15 +204,33 @@ int launch_fwd_f32(const void* q, const void* k, const void* v, void* o, float* 
 template <typename T, int D, int G>
 int launch_decode_g(const attn::decode::Params& p, cudaStream_t st) {
   using namespace attn::decode;
-  static std::atomic<uint64_t> smem_done{0};
-  auto kernel = decode_split_kernel<T, D, G>;
-  constexpr size_t smem = split_smem_bytes<T, D, G>();
-  if (!ensure_smem(kernel, smem, smem_done)) return ATTN_ERR_CUDA;
-  dim3 grid(p.splits, p.Hkv, p.B);
-  kernel<<<grid, kThreads, smem, st>>>(p);
+  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+    // bf16: persistent tensor-core workers, one CTA per SM at most
+    using C = MmaCfg<D, G>;
+    static std::atomic<uint64_t> smem_done{0};
+    auto kernel = decode_split_mma_kernel<D, G>;
+    if (!ensure_smem(kernel, C::kSmemBytes, smem_done)) return ATTN_ERR_CUDA;
+    const long long rows = (long long)p.B * p.Hkv * p.S_max;
+    if (rows >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+    CUtensorMap tk, tv;
+    if (!make_tmap_bf16_2d(&tk, p.kc, D, rows, C::kSub) ||
+        !make_tmap_bf16_2d(&tv, p.vc, D, rows, C::kSub))
+      return ATTN_ERR_CUDA;
+    const long long items = (long long)p.splits * p.B * p.Hkv;
+    long long ctas = std::min<long long>(num_sms(), (items + C::kWarps - 1) / C::kWarps);
+    if (ctas < 1) ctas = 1;
+    launch_pdl(kernel, dim3((unsigned)ctas), dim3(32 * C::kWarps), C::kSmemBytes, st, tk, tv, p);
+  } else {
+    // fp32: one block per (chunk, kv head, sequence) on the CUDA cores
+    static std::atomic<uint64_t> smem_done{0};
+    auto kernel = decode_split_kernel<T, D, G>;
+    constexpr size_t smem = split_smem_bytes<T, D, G>();
+    if (!ensure_smem(kernel, smem, smem_done)) return ATTN_ERR_CUDA;
+    kernel<<<dim3(p.splits, p.Hkv, p.B), kThreads, smem, st>>>(p);
+  }
   int rc = launch_status();
   if (rc != ATTN_OK) return rc;
-  decode_combine_kernel<T, D><<<dim3(p.Hq, p.B), D, 0, st>>>(p);
+  launch_pdl(decode_combine_kernel<T, D>, dim3(p.Hq, p.B), dim3(D), 0, st, p);
   return launch_status();
 }
 

@@ -4,25 +4,30 @@
 // one new query over the S cached positions (the query sits at the last
 // position, so the bottom-right causal mask admits every cached row), and
 // decoding is bandwidth bound because every step reads the whole cache
-// (Cost model).  Grouped-query attention lets the Hq / Hkv query heads of one
-// KV head share a single read of its K and V rows.
+// (Cost model).  Grouped-query attention lets the G = Hq / Hkv query heads of
+// one KV head share a single read of its K and V rows.
 //
-// Pass 1 (decode_split_kernel): one block per (chunk of kChunk keys, kv head,
-// sequence).  The block reads the chunk's K and V rows once for all G query
-// heads of the group and reduces them to a partial result per head: the
-// chunk maximum m (log2 units), denominator l and unnormalised output O.
+// Work is cut into items (chunk of kChunk keys, kv head, sequence); each item
+// is reduced to one partial result per query head: the chunk maximum m (log2
+// units), the denominator l and the unnormalised output O.
+//   bf16: decode_split_mma_kernel -- persistent streaming warps on the tensor
+//         cores (mma.sync m16n8k16), K/V streamed by TMA.
+//   fp32: decode_split_kernel -- one block per item on the CUDA cores, exact
+//         float32 arithmetic.
 // Pass 2 (decode_combine_kernel) merges the partials of every chunk with the
-// online-softmax rescaling exp(m_chunk - m_max) ("Implementing attention from
-// scratch", Stable softmax), normalises, and writes O and LSE.
+// online-softmax rescaling exp2(m_chunk - m_max) ("Implementing attention
+// from scratch", Stable softmax), normalises, and writes O and LSE.
 #pragma once
+
+#include <cuda.h>
 
 #include "common.cuh"
 
 namespace attn {
 namespace decode {
 
-constexpr int kChunk = 256;  // keys per split
-constexpr int kWarps = 8;    // 32 keys per warp
+constexpr int kChunk = 256;  // keys per work item (one partial per item)
+constexpr int kWarps = 8;    // fp32 kernel: 32 keys per warp
 constexpr int kThreads = kWarps * 32;
 
 __host__ __device__ constexpr int max_splits(int S_max) { return (S_max + kChunk - 1) / kChunk; }
@@ -57,8 +62,6 @@ __device__ __forceinline__ void unpack16(const uint4& u, float* f, float*) {
 
 __device__ __forceinline__ float to_f(float x) { return x; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
-
-template <int DPL> struct Lanes;  // DPL consecutive elements of a row per lane
 
 template <typename T, int DPL>
 __device__ __forceinline__ void load_lane(const T* row, int lane, float* f) {
@@ -210,12 +213,348 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Params p) {
   }
 }
 
+// ---------------------------------------------------------------------------
+// bf16 pass 1: persistent streaming workers on the tensor cores.
+//
+// Item virtual index is chunk-major, i = chunk * (B * Hkv) + b * Hkv + g;
+// items whose chunk starts at or past kv_lens[b] are skipped.  Every warp of
+// the grid is an independent worker taking items w, w + W, w + 2W, ... (W
+// workers).  A worker streams its items' keys as 32-key sub-tiles through a
+// private 3-stage ring: K and V arrive as 128B-swizzled TMA tiles (32 rows x
+// 64 columns), the item's q rows by a bulk copy when a new item starts, and
+// two sub-tiles are in flight while the third is computed.
+//
+// Per sub-tile: S = Q K^T with the G query heads as the M = 16 rows of
+// mma.m16n8k16 (rows past G are zero) and K fragments from ldmatrix; the
+// online softmax runs on the accumulator fragments (each thread holds 8
+// scores of rows g and g + 8, the 4 threads of a row group finish the
+// reductions with two shuffles); O += P V reuses the score fragments as the
+// bf16 A operand, with V fragments from ldmatrix.trans.  Scores are scaled
+// in fp32 (scale * log2 e) so that q keeps its exact bf16 values.
+struct Cursor {
+  int item;  // virtual item index, or -1 when the worker's stream is exhausted
+  int j;     // 32-key sub-tile within the item
+  int b, g, chunk, k_begin, k_end, nsub;
+};
+
+__device__ __forceinline__ void cursor_seek(const Params& p, int n_virtual, int stride, int i,
+                                            Cursor& c) {
+  const int bh = p.B * p.Hkv;
+  for (; i < n_virtual; i += stride) {
+    const int chunk = i / bh, bg = i - chunk * bh;
+    const int b = bg / p.Hkv;
+    const int L = min(max(__ldg(p.kv_lens + b), 0), p.S_max);
+    const int k0 = chunk * kChunk;
+    if (k0 < L) {
+      c.item = i;
+      c.j = 0;
+      c.b = b;
+      c.g = bg - b * p.Hkv;
+      c.chunk = chunk;
+      c.k_begin = k0;
+      c.k_end = min(L, k0 + kChunk);
+      c.nsub = (c.k_end - k0 + 31) / 32;
+      return;
+    }
+  }
+  c.item = -1;
+}
+
+__device__ __forceinline__ void cursor_next(const Params& p, int n_virtual, int stride,
+                                            Cursor& c) {
+  if (++c.j < c.nsub) return;
+  cursor_seek(p, n_virtual, stride, c.item + stride, c);
+}
+
+template <int D, int G>
+struct MmaCfg {
+  static constexpr int kSub = 32;                         // keys per sub-tile
+  static constexpr int kStages = 3;
+  static constexpr int kChunks = D / 64;                  // 128-byte column chunks
+  static constexpr uint32_t kTileBytes = kSub * 128;      // one 32 x 64 box
+  static constexpr uint32_t kKBytes = kChunks * kTileBytes;
+  static constexpr uint32_t kStageBytes = 2 * kKBytes;    // K tiles then V tiles
+  static constexpr uint32_t kQRawBytes = (uint32_t)G * D * 2;
+  static constexpr uint32_t kQRawStride = (kQRawBytes + 127) / 128 * 128;
+  static constexpr uint32_t kOffRing = 0;
+  static constexpr uint32_t kOffQRaw = kOffRing + kStages * kStageBytes;
+  static constexpr uint32_t kOffBars = kOffQRaw + 2 * kQRawStride;
+  static constexpr uint32_t kWarpBytes = (kOffBars + 5 * 8 + 1023) / 1024 * 1024;
+  static constexpr int kBudget = 220 * 1024;
+  static constexpr int kWarps = (kBudget / kWarpBytes) > 8 ? 8 : (kBudget / kWarpBytes);
+  static_assert(kWarps >= 1, "decode worker does not fit in shared memory");
+  static constexpr size_t kSmemBytes = (size_t)kWarps * kWarpBytes + 1024;  // + alignment
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                          uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+// d (16x8 fp32) += a (16x16 bf16, row) * b (16x8 bf16, col)
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Byte offset of 16-byte slot c (0..7) of row r in a 128B-swizzled tile.
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(32 * MmaCfg<D, G>::kWarps)
+    decode_split_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, Params p) {
+  using C = MmaCfg<D, G>;
+  constexpr int KS = D / 16;  // k-steps of Q K^T
+  constexpr int NT = D / 8;   // n-tiles of P V
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem_all = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gr = lane >> 2, tq = lane & 3;  // fragment row group, thread in the group
+  uint8_t* smem = smem_all + warp * C::kWarpBytes;
+  const uint32_t ring = smem_u32(smem + C::kOffRing);
+  const uint32_t qraw = smem_u32(smem + C::kOffQRaw);
+  const uint32_t bar_full = smem_u32(smem + C::kOffBars);  // [kStages]
+  const uint32_t bar_q = bar_full + 8 * C::kStages;        // [2]
+
+  if (lane == 0) {
+    for (int i = 0; i < C::kStages + 2; ++i) mbar_init(bar_full + 8 * i, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  // Everything below may read what the previous kernel in the stream wrote.
+  grid_dependency_wait();
+  grid_dependents_launch();
+
+  const int workers = gridDim.x * C::kWarps;
+  const int worker = blockIdx.x * C::kWarps + warp;
+  const int n_virtual = max_splits(p.S_max) * p.B * p.Hkv;
+  Cursor pf, cc;  // prefetch cursor (two sub-tiles ahead) and compute cursor
+  cursor_seek(p, n_virtual, workers, worker, pf);
+  cc = pf;
+  int t_issue = 0, items_issued = 0;
+
+  auto issue = [&](const Cursor& c) {
+    if (lane == 0) {
+      const int row = (c.b * p.Hkv + c.g) * p.S_max + c.k_begin + 32 * c.j;
+      const int st = t_issue % C::kStages;
+      const uint32_t bar = bar_full + 8 * st;
+      const uint32_t dst = ring + st * C::kStageBytes;
+      mbar_arrive_expect_tx(bar, C::kStageBytes);
+#pragma unroll
+      for (int ch = 0; ch < C::kChunks; ++ch) {
+        tma_load_2d(dst + ch * C::kTileBytes, &tm_k, bar, ch * 64, row);
+        tma_load_2d(dst + C::kKBytes + ch * C::kTileBytes, &tm_v, bar, ch * 64, row);
+      }
+      if (c.j == 0) {  // a new item: its q rows too
+        const int qb = items_issued & 1;
+        mbar_arrive_expect_tx(bar_q + 8 * qb, C::kQRawBytes);
+        bulk_load(qraw + qb * C::kQRawStride,
+                  reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                      ((size_t)c.b * p.Hq + (size_t)c.g * G) * D,
+                  C::kQRawBytes, bar_q + 8 * qb);
+      }
+    }
+    if (c.j == 0) ++items_issued;
+    ++t_issue;
+  };
+  for (int k = 0; k < C::kStages - 1 && pf.item >= 0; ++k) {
+    issue(pf);
+    cursor_next(p, n_virtual, workers, pf);
+  }
+
+  uint32_t qa[KS][4];        // Q fragments (rows = heads), fixed per item
+  float o[NT][4];            // O accumulator fragments
+  float m_run[2], l_run[2];  // rows gr and gr + 8 (log2 units)
+  int t = 0, item_seq = 0;
+  bool ok = true;
+  const float sl2 = p.scale_log2;
+  while (cc.item >= 0 && ok) {
+    if (cc.j == 0) {
+      // new item: Q fragments from its q rows; reset the running state
+      const int qb = item_seq & 1;
+      ok = mbar_wait(bar_q + 8 * qb, (item_seq >> 1) & 1, 0x29);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const uint8_t* qs = smem + C::kOffQRaw + qb * C::kQRawStride;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const int c0 = ks * 16 + 2 * tq;
+        qa[ks][0] = (gr < G) ? *reinterpret_cast<const uint32_t*>(qs + (gr * D + c0) * 2) : 0u;
+        qa[ks][2] = (gr < G) ? *reinterpret_cast<const uint32_t*>(qs + (gr * D + c0 + 8) * 2) : 0u;
+        qa[ks][1] = (gr + 8 < G)
+                        ? *reinterpret_cast<const uint32_t*>(qs + ((gr + 8) * D + c0) * 2)
+                        : 0u;
+        qa[ks][3] = (gr + 8 < G)
+                        ? *reinterpret_cast<const uint32_t*>(qs + ((gr + 8) * D + c0 + 8) * 2)
+                        : 0u;
+      }
+#pragma unroll
+      for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+      m_run[0] = m_run[1] = -INFINITY;
+      l_run[0] = l_run[1] = 0.f;
+      ++item_seq;
+      __syncwarp();
+    }
+    if (pf.item >= 0) {  // keep two sub-tiles in flight
+      issue(pf);
+      cursor_next(p, n_virtual, workers, pf);
+    }
+    const int st = t % C::kStages;
+    ok = mbar_wait(bar_full + 8 * st, (t / C::kStages) & 1, 0x2a);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) break;
+    const int nkeys = min(32, cc.k_end - (cc.k_begin + 32 * cc.j));
+    const uint32_t kst = ring + st * C::kStageBytes;
+    const uint32_t vst = kst + C::kKBytes;
+    if (nkeys < 32) {
+      // V rows past the sequence end may hold anything (NaN included): clear
+      // them so that 0 * garbage cannot reach O
+      uint8_t* vt = smem + C::kOffRing + st * C::kStageBytes + C::kKBytes;
+      const int per_chunk = (32 - nkeys) * 8;
+      for (int idx = lane; idx < per_chunk * C::kChunks; idx += 32) {
+        const int ch = idx / per_chunk, rem = idx - ch * per_chunk;
+        *reinterpret_cast<uint4*>(vt + ch * C::kTileBytes + (nkeys + rem / 8) * 128 +
+                                  (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+
+    // S = Q K^T for the 32 keys: 4 n-tiles of 8 keys.
+    float sacc[4][4];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      sacc[nt][0] = sacc[nt][1] = sacc[nt][2] = sacc[nt][3] = 0.f;
+#pragma unroll
+      for (int u = 0; u < KS / 2; ++u) {
+        // four 8x8 matrices: keys 8 nt .. 8 nt + 7, dims 32 u + 8 m
+        const int m = lane >> 3, r = nt * 8 + (lane & 7), cg = 4 * u + m;
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kst + (cg >> 3) * C::kTileBytes + sw128(r, cg & 7), b0, b1, b2, b3);
+        mma_bf16(sacc[nt], qa[2 * u], b0, b1);
+        mma_bf16(sacc[nt], qa[2 * u + 1], b2, b3);
+      }
+    }
+    // Online softmax on the fragments: element e of n-tile nt is row
+    // gr + 8 (e >> 1), key 8 nt + 2 tq + (e & 1).
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = nt * 8 + 2 * tq + (e & 1);
+        const float x = (key < nkeys) ? sacc[nt][e] * sl2 : -INFINITY;
+        sacc[nt][e] = x;
+        mx[e >> 1] = fmaxf(mx[e >> 1], x);
+      }
+    }
+    float alpha[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+      const float mn = fmaxf(m_run[r], mx[r]);
+      alpha[r] = (m_run[r] == -INFINITY) ? 0.f : ex2_approx(m_run[r] - mn);
+      m_run[r] = mn;
+      l_run[r] *= alpha[r];
+    }
+    if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        o[n][0] *= alpha[0];
+        o[n][1] *= alpha[0];
+        o[n][2] *= alpha[1];
+        o[n][3] *= alpha[1];
+      }
+    }
+    uint32_t pa[2][4];  // P as A fragments of the two 16-key k-steps
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      const float p0 = ex2_approx(sacc[nt][0] - m_run[0]);
+      const float p1 = ex2_approx(sacc[nt][1] - m_run[0]);
+      const float p2 = ex2_approx(sacc[nt][2] - m_run[1]);
+      const float p3 = ex2_approx(sacc[nt][3] - m_run[1]);
+      l_run[0] += p0 + p1;
+      l_run[1] += p2 + p3;
+      pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p0, p1);
+      pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2, p3);
+    }
+    // O += P V: 2 k-steps of 16 keys, NT n-tiles of 8 output columns.
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+      for (int v = 0; v < NT / 2; ++v) {
+        const int m = lane >> 3;
+        const int r = ks * 16 + (m & 1) * 8 + (lane & 7), cg = 2 * v + (m >> 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vst + (cg >> 3) * C::kTileBytes + sw128(r, cg & 7), b0, b1, b2, b3);
+        mma_bf16(o[2 * v], pa[ks], b0, b1);
+        mma_bf16(o[2 * v + 1], pa[ks], b2, b3);
+      }
+    }
+    __syncwarp();  // the stage may be refilled from here on
+
+    if (cc.j + 1 == cc.nsub) {
+      // end of the item: one partial per query head of the group
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        float l = l_run[r];
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        const int h = gr + 8 * r;
+        if (h < G) {
+          const size_t slot =
+              ((size_t)cc.b * p.Hq + (size_t)cc.g * G + h) * p.splits + cc.chunk;
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+            *reinterpret_cast<float2*>(p.ws_o + slot * D + n * 8 + 2 * tq) =
+                make_float2(o[n][2 * r], o[n][2 * r + 1]);
+          if (tq == 0) {
+            p.ws_m[slot] = m_run[r];
+            p.ws_l[slot] = l;
+          }
+        }
+      }
+    }
+    cursor_next(p, n_virtual, workers, cc);
+    ++t;
+  }
+  // Drain: every issued copy has landed before the warp exits (immediate
+  // unless a wait above timed out).
+  if (lane == 0) {
+    for (int k = 0; k < C::kStages; ++k) {
+      const int tt = t_issue - 1 - k;
+      if (tt >= 0) mbar_wait(bar_full + 8 * (tt % C::kStages), (tt / C::kStages) & 1, 0x2b);
+    }
+    for (int k = 0; k < 2; ++k) {
+      const int ii = items_issued - 1 - k;
+      if (ii >= 0) mbar_wait(bar_q + 8 * (ii & 1), (ii >> 1) & 1, 0x2c);
+    }
+  }
+}
+
 // Merge the chunk partials of one (b, h): grid (Hq, B), D threads.
 template <typename T, int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(Params p) {
+  __shared__ float sc_s[1024];
+  __shared__ float red[D / 32];
   const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-  const int L = min(max(p.kv_lens[b], 0), p.S_max);
-  const int n = (L + kChunk - 1) / kChunk;
+  grid_dependency_wait();  // the partials come from the split kernel
+  grid_dependents_launch();
+  const int Lb = min(max(p.kv_lens[b], 0), p.S_max);
+  const int n = (Lb + kChunk - 1) / kChunk;
   const size_t row = (size_t)b * p.Hq + h;
   T* o = reinterpret_cast<T*>(p.o) + row * D + d;
   if (n == 0) {
@@ -226,13 +565,32 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(Params p) {
   const float* wm = p.ws_m + row * p.splits;
   const float* wl = p.ws_l + row * p.splits;
   const float* wo = p.ws_o + row * p.splits * D;
-  float M = -INFINITY;
-  for (int s = 0; s < n; ++s) M = fmaxf(M, wm[s]);
-  float acc = 0.f, l = 0.f;
-  for (int s = 0; s < n; ++s) {
-    const float sc = exp2f(wm[s] - M);
-    acc = fmaf(sc, wo[(size_t)s * D + d], acc);
-    l = fmaf(sc, wl[s], l);
+  float acc = 0.f, l = 0.f, M = -INFINITY;
+  for (int base = 0; base < n; base += 1024) {
+    const int cnt = min(1024, n - base);
+    // maximum of this batch of chunk maxima, block-wide
+    float mloc = -INFINITY;
+    for (int s = d; s < cnt; s += D) mloc = fmaxf(mloc, wm[base + s]);
+    mloc = warp_max(mloc);
+    if ((d & 31) == 0) red[d >> 5] = mloc;
+    __syncthreads();
+    float Mb = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < D / 32; ++w) Mb = fmaxf(Mb, red[w]);
+    const float Mn = fmaxf(M, Mb);
+    const float r = (M == -INFINITY) ? 0.f : exp2f(M - Mn);
+    acc *= r;
+    l *= r;
+    M = Mn;
+    for (int s = d; s < cnt; s += D) sc_s[s] = exp2f(wm[base + s] - M);
+    __syncthreads();
+#pragma unroll 8
+    for (int s = 0; s < cnt; ++s) {
+      const float sc = sc_s[s];
+      acc = fmaf(sc, wo[(size_t)(base + s) * D + d], acc);
+      l = fmaf(sc, wl[base + s], l);
+    }
+    __syncthreads();
   }
   store_out(o, acc / l);
   if (p.lse != nullptr && d == 0) p.lse[row] = (M + log2f(l)) * 0.69314718055994531f;
