@@ -163,9 +163,13 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* l
   p.T = T;
   p.S = S;
   p.causal = causal ? 1 : 0;
-  p.n_qtiles = (T + kBM - 1) / kBM;
+  p.n_pairs = (T + kItemRows - 1) / kItemRows;
+  const long long items = (long long)p.n_pairs * B * Hq;
+  if (items >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+  p.n_items = (int)items;
   p.scale_log2 = scale * kLog2e;
-  dim3 grid(p.n_qtiles, Hq, B);
+  // Persistent: one CTA per SM (the kernel takes all 512 TMEM columns).
+  const int grid = (int)std::min<long long>(num_sms(), items);
   kernel<<<grid, kThreads, Cfg<D>::kSmemAlloc, st>>>(tq, tk, tv, p);
   return launch_status();
 }

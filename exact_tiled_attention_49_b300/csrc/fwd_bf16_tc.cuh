@@ -2,23 +2,35 @@
 //
 // The method ("FlashAttention", Transformers in Action section 9.4.1 and
 // Figure 9.8; "Implementing attention from scratch", Core ideas, Stable
-// softmax): a tile of BM query rows stays on chip while BN-key tiles of K and
-// V stream past it; per row a running maximum m and denominator l are kept
-// and the partial output is rescaled by exp(m_old - m_new) when m grows, so
-// the T x S score matrix never reaches HBM.
+// softmax): a tile of query rows stays on chip while 128-key tiles of K and V
+// stream past it; per row a running maximum m and denominator l are kept and
+// the partial output is rescaled by exp(m_old - m_new) when m grows, so the
+// T x S score matrix never reaches HBM.
 //
-// Mapping to sm_103a, one CTA per (query tile, head, batch):
-//   warp 4      TMA producer: Q once, then K_0, K_1, V_0, K_2, V_1, ... into a
-//               ring of NSLOT shared-memory slots (128B-swizzled tiles).
-//   warp 5      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
-//               score buffers (tcgen05.mma, bf16 in, fp32 accumulate), and
-//               O += P_j V_j with P_j read from TMEM as the A operand.
-//   warps 0-3   softmax: thread r owns TMEM lane r = query row r.  It loads
-//               its 128 scores, applies the causal/padding mask on boundary
-//               tiles only, updates m and l, writes P_j = exp2(x - m) as bf16
-//               over the first 64 columns of the score buffer, and rescales
-//               the O row in TMEM when needed.  Epilogue: O / l and the LSE.
-// TMEM (512 columns): S buffers at columns 0 and 128, O at column 256.
+// Mapping to sm_103a.  The kernel is persistent: CTA c handles work items
+// c, c + gridDim.x, ...; an item is a pair of 128-row query tiles (rows q0 ..
+// q0 + 255) of one (batch, head), and items are numbered heaviest first so
+// that causal work balances over the SMs.  Per CTA:
+//   warps 0-3   softmax of query tile 0, warps 4-7 softmax of query tile 1:
+//               thread r of a group owns TMEM lane r = query row r of its
+//               tile.  It loads its 128 scores, masks diagonal/boundary tiles
+//               only, updates m and l, writes P = exp2(x - m) as bf16 over
+//               the first 64 columns of its score buffer, rescales its O row
+//               in TMEM when needed, and at the end of the item writes O / l
+//               and the LSE.
+//   warp 8      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM score
+//               buffer t (tcgen05.mma, bf16 in, fp32 accumulate) and
+//               O_t += P_t V_j with P_t read from TMEM as the A operand.
+//   warp 9      TMA producer: Q_0, Q_1 once per item, then K_0, V_0, K_1,
+//               V_1, ... into a ring of 128B-swizzled shared-memory slots.
+// The two query tiles share every K/V tile and take turns on the tensor
+// cores: while group 0 turns S_0 into P_0, the tensor cores compute P_1 V and
+// the next S_1, and the other way round.  Issue order per key tile j:
+//   PV_0(j), S_0(j+1), PV_1(j), S_1(j+1).
+// tcgen05 operations issued by one thread run in order, so when S_t(j+1) has
+// completed, PV_t(j) has too: the softmax group may rescale O_t right after
+// its score wait, and S_t(j+1) may overwrite the P_t(j) that PV_t(j) read.
+// TMEM (512 columns): S_0 at 0, S_1 at 128, O_0 at 256, O_1 at 256 + D.
 //
 // Rescaling is lazy: the exponent reference m_ref moves only when a row's
 // maximum exceeds it by more than kRescaleThreshold (log2 units), so P can
@@ -33,30 +45,34 @@
 namespace attn {
 namespace tcfwd {
 
-constexpr int kBM = 128;              // query rows per CTA (= TMEM lanes)
+constexpr int kBM = 128;              // query rows per tile (= TMEM lanes)
+constexpr int kQTiles = 2;            // query tiles per work item
+constexpr int kItemRows = kBM * kQTiles;
 constexpr int kBN = 128;              // keys per tile
-constexpr int kThreads = 192;         // 4 softmax warps + load warp + MMA warp
-constexpr int kLoadWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr int kThreads = 320;         // 8 softmax warps + MMA warp + load warp
 constexpr float kRescaleThreshold = 8.0f;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
 
 template <int D>
 struct Cfg {
   static constexpr int kChunks = D / 64;                    // 64-column (128 B) chunks
   static constexpr uint32_t kTileBytes = kBN * D * 2;       // one K or V tile
   static constexpr uint32_t kChunkBytes = kBN * 128;        // 128 rows x 128 B
-  static constexpr uint32_t kQBytes = kBM * D * 2;
+  static constexpr uint32_t kQBytes = kBM * D * 2;          // one query tile
   static constexpr int kSlots = (D == 128) ? 5 : 8;
   static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffSlots = kQBytes;
+  static constexpr uint32_t kOffSlots = kQTiles * kQBytes;
   static constexpr uint32_t kOffBars = kOffSlots + kSlots * kTileBytes;
-  // barriers: q_full, slot_full[S], slot_empty[S], s_full[2], p_full, o_done, drain
-  static constexpr int kNumBars = 1 + 2 * kSlots + 2 + 3;
+  // barriers: q_full[2], q_empty[2], slot_full[S], slot_empty[S], s_full[2],
+  // p_half[2][2], o_full[2], drain
+  static constexpr int kNumBars = 2 + 2 + 2 * kSlots + 2 + 4 + 2 + 1;
   static constexpr uint32_t kOffMisc = kOffBars + 8 * kNumBars;
   static constexpr uint32_t kBytes = kOffMisc + 16;
   static constexpr size_t kSmemAlloc = kBytes + 1024;       // + alignment slack
+  static constexpr uint32_t kColS(int t) { return (uint32_t)(t * kBN); }
+  static constexpr uint32_t kColO(int t) { return (uint32_t)(2 * kBN + t * D); }
 };
 
 struct Params {
@@ -65,21 +81,103 @@ struct Params {
   const int32_t* key_lens;  // [B] or null
   int B, Hq, Hkv, T, S;
   int causal;
-  int n_qtiles;
+  int n_pairs;              // ceil(T / 256)
+  int n_items;              // n_pairs * B * Hq
   float scale_log2;         // scale * log2(e)
 };
 
-// Number of key tiles the query tile starting at q0 must visit, and its valid
-// key bound L.  Shared by all roles so they agree on the trip count.
-__device__ __forceinline__ int tile_count(const Params& p, int b, int q0, int& L) {
-  L = p.S;
-  if (p.key_lens != nullptr) L = min(max(p.key_lens[b], 0), p.S);
+struct Item {
+  int b, h, q0;             // q0 = first row of query tile 0
+};
+
+// Valid key bound L of sequence b.
+__device__ __forceinline__ int key_bound(const Params& p, int b) {
+  return p.key_lens != nullptr ? min(max(p.key_lens[b], 0), p.S) : p.S;
+}
+
+// Number of key tiles the query tile starting at row q0 must visit (0 when
+// every row of the tile is past T, padded, or sees no key).  Every role
+// computes it the same way so they agree on the trip counts.
+__device__ __forceinline__ int tile_count(const Params& p, int q0, int L) {
+  if (q0 >= p.T) return 0;
   const int off = p.S - p.T;
   if (q0 + off >= L) return 0;  // every row of the tile is a padded row
   int kv_end = L;
   if (p.causal) kv_end = min(L, q0 + kBM + off);  // last row sees keys <= q0+BM-1+off
   if (kv_end <= 0) return 0;
   return (kv_end + kBN - 1) / kBN;
+}
+
+// Walks this CTA's work items.  The items are ordered pair-descending (the
+// heaviest causal work first), then by batch and head; a "group" is the Hq
+// items of one (pair, batch).  Items with at least one key tile to visit are
+// dealt out in snake order over the compacted list of such items: CTA c of G
+// takes positions c, 2G-1-c, 2G+c, 4G-1-c, ...  With causal masking and key
+// padding this list is sorted by cost, so the snake keeps the per-SM sums of
+// work within a few percent of each other.  Items with nothing to visit
+// (every row padded or past T) form a second list, dealt out round-robin
+// (c, c+G, ...); their rows are only zeroed.
+//
+// next() is called by a whole converged warp (every lane gets the same
+// item).  Without key padding and with T <= S (or no causal mask) every group
+// is busy and the item follows from its position in closed form; otherwise
+// the warp classifies 32 groups per step (ballot + prefix count), because a
+// serial walk costs about 200 cycles per group.  Every role of the CTA runs
+// its own copy of the iterator and sees the same sequence.
+template <bool kEmpty>
+struct ItemIter {
+  int g0 = 0;           // first group of the current 32-group window
+  int base = 0;         // list index of the window's first item
+  int round = 0;
+
+  __device__ __forceinline__ static void decode(const Params& p, int g, int h, Item& it) {
+    const int pr = g / p.B;
+    it.b = g - pr * p.B;
+    it.h = h;
+    it.q0 = (p.n_pairs - 1 - pr) * kItemRows;
+  }
+
+  __device__ __noinline__ bool next(const Params& p, Item& it) {
+    const int G = gridDim.x, c = blockIdx.x;
+    const int target = kEmpty ? round * G + c : round * G + ((round & 1) ? (G - 1 - c) : c);
+    ++round;
+    const int n_groups = p.n_pairs * p.B;
+    if (p.key_lens == nullptr && (!p.causal || p.T <= p.S)) {  // no group is empty
+      if (kEmpty || target >= n_groups * p.Hq) return false;
+      const int g = target / p.Hq;
+      decode(p, g, target - g * p.Hq, it);
+      return true;
+    }
+    const int lane = threadIdx.x & 31;
+    for (; g0 < n_groups; g0 += 32) {
+      const int g = g0 + lane;
+      bool in_list = false;
+      if (g < n_groups) {
+        const int pr = g / p.B, b = g - pr * p.B;
+        const int q0 = (p.n_pairs - 1 - pr) * kItemRows;
+        const int L = key_bound(p, b);
+        const bool busy = tile_count(p, q0, L) > 0 || tile_count(p, q0 + kBM, L) > 0;
+        in_list = busy != kEmpty;
+      }
+      const uint32_t mask = __ballot_sync(0xffffffffu, in_list);
+      const int cnt = __popc(mask) * p.Hq;
+      if (target < base + cnt) {
+        const int k = (target - base) / p.Hq;
+        const bool mine = in_list && __popc(mask & ((1u << lane) - 1u)) == k;
+        const int sel = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+        decode(p, g0 + sel, target - base - k * p.Hq, it);
+        return true;  // later targets are larger: keep this window
+      }
+      base += cnt;
+    }
+    return false;
+  }
+};
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 template <int D>
@@ -95,35 +193,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_q = sbase + C::kOffQ;
   const uint32_t s_slots = sbase + C::kOffSlots;
   const uint32_t bars = sbase + C::kOffBars;
-  const uint32_t bar_q = bars;
-  auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
-  auto bar_empty = [&](int s) { return bars + 8u * (1 + C::kSlots + s); };
-  const uint32_t bar_s0 = bars + 8u * (1 + 2 * C::kSlots);
-  const uint32_t bar_p = bar_s0 + 16;
-  const uint32_t bar_o = bar_p + 8;
-  const uint32_t bar_drain = bar_o + 8;
+  auto bar_qfull = [&](int t) { return bars + 8u * t; };
+  auto bar_qempty = [&](int t) { return bars + 8u * (2 + t); };
+  auto bar_full = [&](int s) { return bars + 8u * (4 + s); };
+  auto bar_empty = [&](int s) { return bars + 8u * (4 + C::kSlots + s); };
+  const uint32_t bar_s = bars + 8u * (4 + 2 * C::kSlots);  // s_full[t] = bar_s + 8t
+  const uint32_t bar_p = bar_s + 16;                        // p_half[t][h] = bar_p + 16t + 8h
+  const uint32_t bar_o = bar_p + 32;                        // o_full[t]
+  const uint32_t bar_drain = bar_o + 16;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = p.n_qtiles - 1 - (int)blockIdx.x;  // heaviest causal tiles first
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int g = h / (p.Hq / p.Hkv);
-  const int q0 = qt * kBM;
-  int L;
-  const int n = tile_count(p, b, q0, L);
   const int off = p.S - p.T;
 
   if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(bar_qfull(t), 1);
+      mbar_init(bar_qempty(t), 1);
+      mbar_init(bar_s + 8 * t, 1);
+      mbar_init(bar_p + 16 * t, 4 * 32);
+      mbar_init(bar_p + 16 * t + 8, 4 * 32);
+      mbar_init(bar_o + 8 * t, 1);
+    }
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(bar_full(s), 1);
       mbar_init(bar_empty(s), 1);
     }
-    mbar_init(bar_s0, 1);
-    mbar_init(bar_s0 + 8, 1);
-    mbar_init(bar_p, 4 * 32);
-    mbar_init(bar_o, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -139,225 +235,354 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kLoadWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n > 0) {
+    // The whole warp walks the schedule and waits; lane 0 issues the copies.
+    if (lane == 0) {
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
-      const int bh_q = b * p.Hq + h;
-      const int bh_kv = b * p.Hkv + g;
-      mbar_arrive_expect_tx(bar_q, C::kQBytes);
-      for (int c = 0; c < C::kChunks; ++c)
-        tma_load_3d(s_q + c * C::kChunkBytes, &tm_q, bar_q, c * 64, q0, bh_q);
-      // Load order = consumption order: K_0, then (K_j, V_{j-1}) for j >= 1,
-      // then V_{n-1}.
-      const int total = 2 * n;
-      int last_issue[C::kSlots];
-      for (int s = 0; s < C::kSlots; ++s) last_issue[s] = -1;
-      for (int t = 0; t < total; ++t) {
-        bool is_v;
-        int tile;
-        if (t == 0) { is_v = false; tile = 0; }
-        else if (t == total - 1) { is_v = true; tile = n - 1; }
-        else if (t & 1) { is_v = false; tile = (t + 1) >> 1; }
-        else { is_v = true; tile = (t >> 1) - 1; }
-        const int slot = t % C::kSlots;
-        if (t >= C::kSlots) {
-          if (!mbar_wait(bar_empty(slot), ((t / C::kSlots) - 1) & 1, 1, abort_flag)) break;
-        }
-        const uint32_t dst = s_slots + slot * C::kTileBytes;
-        mbar_arrive_expect_tx(bar_full(slot), C::kTileBytes);
-        const CUtensorMap* tm = is_v ? &tm_v : &tm_k;
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(dst + c * C::kChunkBytes, tm, bar_full(slot), c * 64, tile * kBN, bh_kv);
-        last_issue[slot] = t;
-      }
-      // Drain: every issued copy must land before the CTA may exit.
-      for (int s = 0; s < C::kSlots; ++s)
-        if (last_issue[s] >= 0) mbar_wait(bar_full(s), (last_issue[s] / C::kSlots) & 1, 2);
     }
+    int ring = 0, qi = 0;
+    bool ok = true;
+    auto wait_bar = [&](uint32_t bar, uint32_t parity) {
+      const bool w = mbar_wait(bar, parity, 1, abort_flag);
+      return __all_sync(0xffffffffu, w);
+    };
+    ItemIter<false> iter;
+    Item it;
+    while (ok && iter.next(p, it)) {
+      const int L = key_bound(p, it.b);
+      const int n0 = tile_count(p, it.q0, L), n1 = tile_count(p, it.q0 + kBM, L);
+      const int nm = max(n0, n1);
+      if (nm == 0) continue;
+      const int bh_q = it.b * p.Hq + it.h;
+      const int bh_kv = it.b * p.Hkv + it.h / (p.Hq / p.Hkv);
+      for (int t = 0; t < kQTiles && ok; ++t) {
+        if (qi > 0) ok = wait_bar(bar_qempty(t), (qi - 1) & 1);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar_qfull(t), C::kQBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(s_q + t * C::kQBytes + c * C::kChunkBytes, &tm_q, bar_qfull(t), c * 64,
+                        it.q0 + t * kBM, bh_q);
+        }
+      }
+      ++qi;
+      // K_0, V_0, K_1, V_1, ...: the order the MMA warp consumes them.
+      for (int u = 0; ok && u < 2 * nm; ++u) {
+        const int slot = ring % C::kSlots;
+        if (ring >= C::kSlots) ok = wait_bar(bar_empty(slot), ((ring / C::kSlots) - 1) & 1);
+        if (!ok) break;
+        if (lane == 0) {
+          const uint32_t dst = s_slots + slot * C::kTileBytes;
+          mbar_arrive_expect_tx(bar_full(slot), C::kTileBytes);
+          const CUtensorMap* tm = (u & 1) ? &tm_v : &tm_k;
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(dst + c * C::kChunkBytes, tm, bar_full(slot), c * 64, (u >> 1) * kBN,
+                        bh_kv);
+        }
+        ++ring;
+      }
+    }
+    // Drain: every issued copy must land before the CTA may exit (the last
+    // kSlots ring entries cover every slot's latest copy).
+    for (int u = max(0, ring - C::kSlots); u < ring; ++u)
+      mbar_wait(bar_full(u % C::kSlots), (u / C::kSlots) & 1, 3);
+    if (qi > 0)
+      for (int t = 0; t < kQTiles; ++t) mbar_wait(bar_qfull(t), (qi - 1) & 1, 3);
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0 && n > 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, false, true);
-      bool ok = mbar_wait(bar_q, 0, 3, abort_flag);
-      int t = 0;  // consumption counter (same order as the loads)
-      auto wait_slot = [&](int tt) {
-        return mbar_wait(bar_full(tt % C::kSlots), (tt / C::kSlots) & 1, 4, abort_flag);
-      };
-      auto issue_qk = [&](int tt, int buf) {
-        const uint32_t kt = s_slots + (tt % C::kSlots) * C::kTileBytes;
-        const uint32_t d_tmem = tmem + (buf ? kColS1 : kColS0);
+    // The whole warp walks the schedule; one elected lane issues each
+    // tcgen05 instruction.  Descriptors are built once per base address and
+    // advanced by constants, so every MMA costs only its issue slot.
+    constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, false, false);
+    constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, false, true);
+    const uint64_t dq0 = sdesc_sw128(s_q, 16, 1024);                // Q_0 as the A operand
+    const uint64_t dk0 = sdesc_sw128(s_slots, 16, 1024);            // slot 0 as K (K-major B)
+    const uint64_t dv0 = sdesc_sw128(s_slots, C::kChunkBytes, 1024);  // slot 0 as V (MN-major B)
+    int ring = 0, qi = 0;
+    uint32_t np0 = 0, np1 = 0;  // p_half waits so far, per tile
+    bool ok = true;
+    auto wait_slot = [&](int r) {
+      const bool w = mbar_wait(bar_full(r % C::kSlots), (r / C::kSlots) & 1, 4, abort_flag);
+      return __all_sync(0xffffffffu, w);
+    };
+    auto wait_bar = [&](uint32_t bar, uint32_t parity) {
+      const bool w = mbar_wait(bar, parity, 6, abort_flag);
+      return __all_sync(0xffffffffu, w);
+    };
+    // S_t = Q_t K^T for the K tile in `slot`.  The start-address field of a
+    // descriptor is address >> 4 in its low 14 bits; shared addresses stay
+    // below 2^18, so adding byte offsets >> 4 never carries out of it.
+    auto issue_qk = [&](int t, int slot) {
+      const uint64_t dq = dq0 + (uint64_t)((t * C::kQBytes) >> 4);
+      const uint64_t dk = dk0 + (uint64_t)((slot * C::kTileBytes) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-          umma_ss(d_tmem, sdesc_sw128(s_q + koff, 16, 1024), sdesc_sw128(kt + koff, 16, 1024),
-                  idesc_qk, kk > 0);
-        }
-        umma_commit(bar_s0 + 8 * buf);
-        umma_commit(bar_empty(tt % C::kSlots));
-      };
-      if (ok && (ok = wait_slot(t))) {
-        tc_fence_after();
-        issue_qk(t, 0);
-        ++t;
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
+        umma_ss_elect(tmem + C::kColS(t), dq + koff, dk + koff, idesc_qk, kk > 0);
       }
-      for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n) {
-          if (!(ok = wait_slot(t))) break;
+      umma_commit_elect(bar_s + 8 * t);
+    };
+    // O_t += P_t V for keys [64 * half, 64 * half + 64) of the tile in `slot`.
+    auto issue_pv = [&](int t, int slot, int half, bool acc) {
+      const uint64_t dv = dv0 + (uint64_t)((slot * C::kTileBytes) >> 4);
+#pragma unroll
+      for (int k4 = 0; k4 < kBN / 32; ++k4) {
+        const int kk = half * (kBN / 32) + k4;
+        umma_ts_elect(tmem + C::kColO(t), tmem + C::kColS(t) + kk * 8, dv + (uint64_t)(kk * 128),
+                      idesc_pv, (acc || kk > 0) ? 1u : 0u);
+      }
+    };
+    ItemIter<false> iter;
+    Item it;
+    while (ok && iter.next(p, it)) {
+      const int L = key_bound(p, it.b);
+      const int n0 = tile_count(p, it.q0, L), n1 = tile_count(p, it.q0 + kBM, L);
+      const int nm = max(n0, n1);
+      if (nm == 0) continue;
+      ok = wait_bar(bar_qfull(0), qi & 1) && wait_bar(bar_qfull(1), qi & 1);
+      ++qi;
+      if (!ok) break;
+      // K_0: the first score tile of both query tiles.
+      int kslot = ring % C::kSlots;
+      if (!(ok = wait_slot(ring))) break;
+      ++ring;
+      tc_fence_after();
+#pragma unroll
+      for (int t = 0; t < kQTiles; ++t) {
+        const int nt = t ? n1 : n0;
+        if (nt > 0) issue_qk(t, kslot);
+        if (nt <= 1) umma_commit_elect(bar_qempty(t));  // Q_t read for the last time
+      }
+      umma_commit_elect(bar_empty(kslot));
+      for (int j = 0; ok && j < nm; ++j) {
+        const int vslot = ring % C::kSlots;
+        if (!(ok = wait_slot(ring))) break;
+        ++ring;
+        const bool has_next = j + 1 < nm;
+        bool next_ready = false;
+        kslot = ring % C::kSlots;
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < kQTiles; ++t) {
+          const int nt = t ? n1 : n0;
+          if (j >= nt) continue;
+          uint32_t& npt = t ? np1 : np0;
+          // P_t arrives in two halves; the first half's MMAs run while the
+          // softmax group still computes the second.
+          if (!(ok = wait_bar(bar_p + 16 * t, npt & 1))) break;
           tc_fence_after();
-          issue_qk(t, (j + 1) & 1);
-          ++t;
+          issue_pv(t, vslot, 0, j > 0);
+          if (!(ok = wait_bar(bar_p + 16 * t + 8, npt & 1))) break;
+          ++npt;
+          tc_fence_after();
+          issue_pv(t, vslot, 1, true);
+          if (j + 1 < nt) {
+            if (!next_ready) {
+              if (!(ok = wait_slot(ring))) break;
+              next_ready = true;
+              tc_fence_after();
+            }
+            issue_qk(t, kslot);
+            if (j + 2 == nt) umma_commit_elect(bar_qempty(t));
+          } else {
+            umma_commit_elect(bar_o + 8 * t);  // O_t complete for this item
+          }
         }
-        if (!(ok = mbar_wait(bar_p, j & 1, 5, abort_flag))) break;
-        if (!(ok = wait_slot(t))) break;
-        tc_fence_after();
-        const uint32_t vt = s_slots + (t % C::kSlots) * C::kTileBytes;
-        const uint32_t p_tmem = tmem + ((j & 1) ? kColS1 : kColS0);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          umma_ts(tmem + kColO, p_tmem + kk * 8, sdesc_sw128(vt + kk * 2048, C::kChunkBytes, 1024),
-                  idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        if (!ok) break;
+        umma_commit_elect(bar_empty(vslot));
+        if (has_next) {
+          // K_{j+1} is consumed by at least one tile because j + 1 < nm.
+          umma_commit_elect(bar_empty(kslot));
+          ++ring;
         }
-        umma_commit(bar_o);
-        umma_commit(bar_empty(t % C::kSlots));
-        ++t;
       }
-      // Drain: all issued MMAs complete before TMEM is released.
-      umma_commit(bar_drain);
-      mbar_wait(bar_drain, 0, 6);
     }
+    // Drain: all issued MMAs complete before TMEM is released.
+    umma_commit_elect(bar_drain);
+    mbar_wait(bar_drain, 0, 7);
     __syncwarp();
   } else {
     // ------------------------------------------------------------- softmax
-    const int r = threadIdx.x;  // query row within the tile = TMEM lane
-    const int i = q0 + r;
-    const int pos = i + off;
-    const bool row_ok = (i < p.T) && (pos < L);
-    const int lim = p.causal ? min(L, pos + 1) : L;  // visible keys: [0, lim)
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const int t = warp >> 2;                  // query tile of this group
+    const int r = ((warp & 3) << 5) | lane;   // row within the tile = TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t ts = lane_base + C::kColS(t);
+    const uint32_t to = lane_base + C::kColO(t);
+    const uint32_t bar_st = bar_s + 8 * t, bar_pt = bar_p + 16 * t, bar_ot = bar_o + 8 * t;
     const float sl2 = p.scale_log2;
-    float m_ref = -INFINITY;  // exponent reference (log2 units)
-    float l = 0.f;
+    uint32_t ns = 0, no = 0;                  // s_full / o_full waits so far
     bool ok = true;
 
-    for (int j = 0; j < n; ++j) {
-      const int buf = j & 1;
-      ok = mbar_wait(bar_s0 + 8 * buf, (j >> 1) & 1, 7, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const uint32_t ts = lane_base + (buf ? kColS1 : kColS0);
-      uint32_t sr[kBN];
-      tmem_ld32(ts + 0, sr + 0);
-      tmem_ld32(ts + 32, sr + 32);
-      tmem_ld32(ts + 64, sr + 64);
-      tmem_ld32(ts + 96, sr + 96);
-      tmem_wait_ld32(sr + 0);
-      tmem_wait_ld32(sr + 32);
-      tmem_wait_ld32(sr + 64);
-      tmem_wait_ld32(sr + 96);
+    ItemIter<false> iter;
+    Item it;
+    while (ok && iter.next(p, it)) {
+      const int L = key_bound(p, it.b);
+      const int q0t = it.q0 + t * kBM;
+      const int n = tile_count(p, q0t, L);
+      const int i = q0t + r;
+      const int pos = i + off;
+      const bool row_ok = (i < p.T) && (pos < L);
+      const int lim = p.causal ? min(L, pos + 1) : L;  // visible keys: [0, lim)
+      float m_ref = -INFINITY;  // exponent reference (log2 units)
+      float l = 0.f;
 
-      const int k0 = j * kBN;
-      const bool masked = (k0 + kBN > L) || (p.causal && (k0 + kBN - 1 > q0 + off));
-      float mx = -INFINITY;
-      if (masked) {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          if (k0 + c >= lim) sr[c] = __float_as_uint(-INFINITY);
-          mx = fmaxf(mx, __uint_as_float(sr[c]));
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
-      }
-      const float m_tile = mx * sl2;  // -inf stays -inf (sl2 > 0)
-
-      // Lazy rescale: move the reference only when the maximum ran ahead.
-      const bool first = (m_ref == -INFINITY);
-      const bool grow = !first && (m_tile > m_ref + kRescaleThreshold);
-      if (first && m_tile != -INFINITY) m_ref = m_tile;
-      if (__any_sync(0xffffffffu, grow)) {
-        // O holds P_{j-1} V_{j-1} only once that MMA has completed.
-        ok = mbar_wait(bar_o, (j - 1) & 1, 8, abort_flag);
+      for (int j = 0; j < n; ++j) {
+        ok = mbar_wait(bar_st, ns & 1, 8, abort_flag);
+        ++ns;
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        const float alpha = grow ? ex2_approx(m_ref - m_tile) : 1.f;
+        uint32_t sr[kBN];
+        tmem_ld32(ts + 0, sr + 0);
+        tmem_ld32(ts + 32, sr + 32);
+        tmem_ld32(ts + 64, sr + 64);
+        tmem_ld32(ts + 96, sr + 96);
+        tmem_wait_ld32(sr + 0);
+        tmem_wait_ld32(sr + 32);
+        tmem_wait_ld32(sr + 64);
+        tmem_wait_ld32(sr + 96);
+
+        const int k0 = j * kBN;
+        const bool masked = (k0 + kBN > L) || (p.causal && (k0 + kBN - 1 > q0t + off));
+        if (masked) {
+#pragma unroll
+          for (int c = 0; c < kBN; ++c)
+            if (k0 + c >= lim) sr[c] = __float_as_uint(-INFINITY);
+        }
+        // Row maximum: eight independent chains of three-input max.
+        float mx[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kBN; c += 16) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            mx[e] = max3f(mx[e], __uint_as_float(sr[c + 2 * e]), __uint_as_float(sr[c + 2 * e + 1]));
+        }
+        const float m_tile =
+            max3f(max3f(mx[0], mx[1], mx[2]), max3f(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) *
+            sl2;  // -inf stays -inf
+        // Lazy rescale: move the reference only when the maximum ran ahead.
+        const bool first = (m_ref == -INFINITY);
+        const bool grow = !first && (m_tile > m_ref + kRescaleThreshold);
+        float alpha = 1.f;
+        if (first && m_tile != -INFINITY) m_ref = m_tile;
         if (grow) {
+          alpha = ex2_approx(m_ref - m_tile);
           l *= alpha;
           m_ref = m_tile;
         }
+
+        // P = exp2(s * scale * log2e - m_ref), packed to bf16 pairs, in two
+        // halves of 64 keys; each half is released to the MMA warp on its own.
+        const float neg_ref = (m_ref == -INFINITY) ? 0.f : -m_ref;
+        const float2 sl2x2 = make_float2(sl2, sl2);
+        const float2 negx2 = make_float2(neg_ref, neg_ref);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
+        uint32_t pk[kBN / 2];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+#pragma unroll
+          for (int c = half * 64; c < half * 64 + 64; c += 8) {
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+              const float2 x = __ffma2_rn(
+                  make_float2(__uint_as_float(sr[c + e]), __uint_as_float(sr[c + e + 1])), sl2x2,
+                  negx2);
+              const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              pk[(c + e) >> 1] = pack_bf16x2(pe.x, pe.y);
+              if (e == 0) acc0 = __fadd2_rn(acc0, pe);
+              else if (e == 2) acc1 = __fadd2_rn(acc1, pe);
+              else if (e == 4) acc2 = __fadd2_rn(acc2, pe);
+              else acc3 = __fadd2_rn(acc3, pe);
+            }
+          }
+          tmem_st32(ts + 32 * half, pk + 32 * half);
+          if (half == 0) {
+            // O_t is final up to key tile j-1 here: PV_t(j-1) was issued
+            // before S_t(j), whose completion this group has seen.  PV_t(j)
+            // starts only after the arrive below, so it adds to the rescaled
+            // row.
+            if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+              for (int c = 0; c < D / 32; ++c) {
+                uint32_t orr[32];
+                tmem_ld32(to + 32 * c, orr);
+                tmem_wait_ld32(orr);
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                  orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+                tmem_st32(to + 32 * c, orr);
+              }
+            }
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(bar_pt + 8 * half);
+        }
+        const float2 s01 = __fadd2_rn(acc0, acc1), s23 = __fadd2_rn(acc2, acc3);
+        const float2 s4 = __fadd2_rn(s01, s23);
+        l += s4.x + s4.y;
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- epilogue
+      if (n > 0) {
+        ok = mbar_wait(bar_ot, no & 1, 9, abort_flag);
+        ++no;
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      const bool has = row_ok && (l > 0.f);
+      const float inv = has ? 1.f / l : 0.f;
+      __nv_bfloat16* orow =
+          reinterpret_cast<__nv_bfloat16*>(p.o) + ((((size_t)it.b * p.Hq + it.h) * p.T) + i) * D;
+      if (__any_sync(0xffffffffu, has)) {
+        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t orr[32];
-          tmem_ld32(lane_base + kColO + 32 * c, orr);
+          tmem_ld32(to + 32 * c, orr);
           tmem_wait_ld32(orr);
+          if (i < p.T) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-          tmem_st32(lane_base + kColO + 32 * c, orr);
-        }
-      }
-
-      const float neg_ref = (m_ref == -INFINITY) ? 0.f : -m_ref;
-      float sum = 0.f;
-      uint32_t pk[kBN / 2];
-#pragma unroll
-      for (int c = 0; c < kBN; c += 2) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), sl2, neg_ref));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), sl2, neg_ref));
-        sum += p0 + p1;
-        pk[c >> 1] = pack_bf16x2(p0, p1);
-      }
-      l += sum;
-      tmem_st32(ts + 0, pk);
-      tmem_st32(ts + 32, pk + 32);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_p);
-    }
-
-    // ------------------------------------------------------------ epilogue
-    if (ok && n > 0) {
-      ok = mbar_wait(bar_o, (n - 1) & 1, 9, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    const bool has = ok && row_ok && (l > 0.f);
-    const float inv = has ? 1.f / l : 0.f;
-    __nv_bfloat16* orow =
-        reinterpret_cast<__nv_bfloat16*>(p.o) + ((((size_t)b * p.Hq + h) * p.T) + i) * D;
-    if (__any_sync(0xffffffffu, has)) {
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t orr[32];
-        tmem_ld32(lane_base + kColO + 32 * c, orr);
-        tmem_wait_ld32(orr);
-        if (!has) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) orr[e] = 0u;
-        }
-        if (i < p.T) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 u;
-            u.x = pack_bf16x2(__uint_as_float(orr[8 * v + 0]) * inv, __uint_as_float(orr[8 * v + 1]) * inv);
-            u.y = pack_bf16x2(__uint_as_float(orr[8 * v + 2]) * inv, __uint_as_float(orr[8 * v + 3]) * inv);
-            u.z = pack_bf16x2(__uint_as_float(orr[8 * v + 4]) * inv, __uint_as_float(orr[8 * v + 5]) * inv);
-            u.w = pack_bf16x2(__uint_as_float(orr[8 * v + 6]) * inv, __uint_as_float(orr[8 * v + 7]) * inv);
-            dst[v] = u;
+            for (int v = 0; v < 4; ++v) {
+              uint4 u;
+              u.x = pack_bf16x2(__uint_as_float(orr[8 * v + 0]) * inv,
+                                __uint_as_float(orr[8 * v + 1]) * inv);
+              u.y = pack_bf16x2(__uint_as_float(orr[8 * v + 2]) * inv,
+                                __uint_as_float(orr[8 * v + 3]) * inv);
+              u.z = pack_bf16x2(__uint_as_float(orr[8 * v + 4]) * inv,
+                                __uint_as_float(orr[8 * v + 5]) * inv);
+              u.w = pack_bf16x2(__uint_as_float(orr[8 * v + 6]) * inv,
+                                __uint_as_float(orr[8 * v + 7]) * inv);
+              dst[v] = u;
+            }
           }
         }
+        tc_fence_before();
+      } else if (i < p.T) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+        for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
       }
-    } else if (i < p.T) {
-      uint4* dst = reinterpret_cast<uint4*>(orow);
-      for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+      if (p.lse != nullptr && i < p.T) {
+        p.lse[((size_t)it.b * p.Hq + it.h) * p.T + i] =
+            has ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+      }
     }
-    if (p.lse != nullptr && i < p.T) {
-      p.lse[((size_t)b * p.Hq + h) * p.T + i] =
-          has ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+    // Items with no key tile: every row is padded (or past T): O = 0, LSE = -inf.
+    ItemIter<true> empty;
+    while (ok && empty.next(p, it)) {
+      const int i = it.q0 + t * kBM + r;
+      if (i >= p.T) continue;
+      const size_t row = ((size_t)it.b * p.Hq + it.h) * p.T + i;
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + row * D);
+#pragma unroll
+      for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
+      if (p.lse != nullptr) p.lse[row] = -INFINITY;
     }
   }
 
