@@ -167,6 +167,7 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* l
   const long long items = (long long)p.n_pairs * B * Hq;
   if (items >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
   p.n_items = (int)items;
+  p.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
   p.scale_log2 = scale * kLog2e;
   // Persistent: one CTA per SM (the kernel takes all 512 TMEM columns).
   const int grid = (int)std::min<long long>(num_sms(), items);

@@ -68,8 +68,10 @@ struct Cfg {
   // barriers: q_full[2], q_empty[2], slot_full[S], slot_empty[S], s_full[2],
   // p_half[2][2], o_full[2], drain
   static constexpr int kNumBars = 2 + 2 + 2 * kSlots + 2 + 4 + 2 + 1;
-  static constexpr uint32_t kOffMisc = kOffBars + 8 * kNumBars;
-  static constexpr uint32_t kBytes = kOffMisc + 16;
+  static constexpr uint32_t kOffMisc = kOffBars + 8 * kNumBars;    // TMEM address, abort flag
+  static constexpr uint32_t kOffSched = (kOffMisc + 16 + 15) / 16 * 16;  // SchedArgs
+  static constexpr uint32_t kOffWalk = kOffSched + 48;                   // WalkState[warps][2]
+  static constexpr uint32_t kBytes = kOffWalk + 16 * 2 * (kThreads / 32);
   static constexpr size_t kSmemAlloc = kBytes + 1024;       // + alignment slack
   static constexpr uint32_t kColS(int t) { return (uint32_t)(t * kBN); }
   static constexpr uint32_t kColO(int t) { return (uint32_t)(2 * kBN + t * D); }
@@ -83,6 +85,7 @@ struct Params {
   int causal;
   int n_pairs;              // ceil(T / 256)
   int n_items;              // n_pairs * B * Hq
+  int o_align32;            // o is 32-byte aligned: 256-bit stores
   float scale_log2;         // scale * log2(e)
 };
 
@@ -108,71 +111,107 @@ __device__ __forceinline__ int tile_count(const Params& p, int q0, int L) {
   return (kv_end + kBN - 1) / kBN;
 }
 
-// Walks this CTA's work items.  The items are ordered pair-descending (the
-// heaviest causal work first), then by batch and head; a "group" is the Hq
-// items of one (pair, batch).  Items with at least one key tile to visit are
-// dealt out in snake order over the compacted list of such items: CTA c of G
-// takes positions c, 2G-1-c, 2G+c, 4G-1-c, ...  With causal masking and key
-// padding this list is sorted by cost, so the snake keeps the per-SM sums of
-// work within a few percent of each other.  Items with nothing to visit
-// (every row padded or past T) form a second list, dealt out round-robin
-// (c, c+G, ...); their rows are only zeroed.
-//
-// next() is called by a whole converged warp (every lane gets the same
-// item).  Without key padding and with T <= S (or no causal mask) every group
-// is busy and the item follows from its position in closed form; otherwise
-// the warp classifies 32 groups per step (ballot + prefix count), because a
-// serial walk costs about 200 cycles per group.  Every role of the CTA runs
-// its own copy of the iterator and sees the same sequence.
-template <bool kEmpty>
-struct ItemIter {
-  int g0 = 0;           // first group of the current 32-group window
-  int base = 0;         // list index of the window's first item
-  int round = 0;
-
-  __device__ __forceinline__ static void decode(const Params& p, int g, int h, Item& it) {
-    const int pr = g / p.B;
-    it.b = g - pr * p.B;
-    it.h = h;
-    it.q0 = (p.n_pairs - 1 - pr) * kItemRows;
-  }
-
-  __device__ __noinline__ bool next(const Params& p, Item& it) {
-    const int G = gridDim.x, c = blockIdx.x;
-    const int target = kEmpty ? round * G + c : round * G + ((round & 1) ? (G - 1 - c) : c);
-    ++round;
-    const int n_groups = p.n_pairs * p.B;
-    if (p.key_lens == nullptr && (!p.causal || p.T <= p.S)) {  // no group is empty
-      if (kEmpty || target >= n_groups * p.Hq) return false;
-      const int g = target / p.Hq;
-      decode(p, g, target - g * p.Hq, it);
-      return true;
-    }
-    const int lane = threadIdx.x & 31;
-    for (; g0 < n_groups; g0 += 32) {
-      const int g = g0 + lane;
-      bool in_list = false;
-      if (g < n_groups) {
-        const int pr = g / p.B, b = g - pr * p.B;
-        const int q0 = (p.n_pairs - 1 - pr) * kItemRows;
-        const int L = key_bound(p, b);
-        const bool busy = tile_count(p, q0, L) > 0 || tile_count(p, q0 + kBM, L) > 0;
-        in_list = busy != kEmpty;
-      }
-      const uint32_t mask = __ballot_sync(0xffffffffu, in_list);
-      const int cnt = __popc(mask) * p.Hq;
-      if (target < base + cnt) {
-        const int k = (target - base) / p.Hq;
-        const bool mine = in_list && __popc(mask & ((1u << lane) - 1u)) == k;
-        const int sel = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
-        decode(p, g0 + sel, target - base - k * p.Hq, it);
-        return true;  // later targets are larger: keep this window
-      }
-      base += cnt;
-    }
-    return false;
-  }
+// Sizes the work walk needs, copied once into shared memory, and one walk
+// state per warp.  The walk is a non-inlined function that takes only
+// shared-memory pointers: passing the kernel parameters by reference to a
+// non-inlined function would move them to local memory, and every later
+// parameter read in the kernel would become a slow local load.
+struct SchedArgs {
+  const int32_t* key_lens;
+  int n_pairs, B, Hq, T, S, causal, all_busy;
 };
+struct WalkState {
+  int g0;       // first group of the current 32-group window
+  int base;     // list index of the window's first item
+  int round;    // items handed out so far
+  int pad;
+};
+
+// Key tiles of the query tile starting at q0 (the rule of tile_count).
+__device__ __forceinline__ int sched_tiles(const SchedArgs& a, int q0, int L) {
+  if (q0 >= a.T || q0 + a.S - a.T >= L) return 0;
+  const int kv_end = a.causal ? min(L, q0 + kBM + a.S - a.T) : L;
+  return kv_end <= 0 ? 0 : (kv_end + kBN - 1) / kBN;
+}
+
+// Next work item of this CTA, packed as valid << 63 | pair << 32 | b << 16 | h
+// (0 when there is none).
+//
+// The items are ordered pair-descending (the heaviest causal work first),
+// then by batch and head; a "group" is the Hq items of one (pair, batch).
+// Items with at least one key tile to visit are dealt out in snake order over
+// the compacted list of such items: CTA c of G takes positions c, 2G-1-c,
+// 2G+c, 4G-1-c, ...  With causal masking and key padding this list is
+// sorted by cost, so the snake keeps the per-SM sums of work within a few
+// percent of each other.  Items with nothing to visit (every row padded or
+// past T) form a second list (kEmpty), dealt out round-robin (c, c+G, ...);
+// their rows are only zeroed.
+//
+// Called by a whole converged warp; every lane gets the same item.  Without
+// key padding and with T <= S (or no causal mask) no group is empty and the
+// item follows from its position in closed form; otherwise the warp
+// classifies 32 groups per step (ballot + prefix count), because a serial
+// walk costs about 200 cycles per group.  Every role of the CTA walks its
+// own copy and sees the same sequence.
+template <bool kEmpty>
+__device__ __noinline__ uint64_t sched_next(const SchedArgs* args, WalkState* st) {
+  const SchedArgs a = *args;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int round = st->round;
+  const int target = kEmpty ? round * G + c : round * G + ((round & 1) ? (G - 1 - c) : c);
+  const int n_groups = a.n_pairs * a.B;
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  if (lane == 0) st->round = round + 1;
+  if (a.all_busy) {
+    __syncwarp();
+    if (kEmpty || target >= n_groups * a.Hq) return 0;
+    const int g = target / a.Hq;
+    const int pr = g / a.B;
+    return (1ull << 63) | ((uint64_t)(a.n_pairs - 1 - pr) << 32) |
+           ((uint64_t)(g - pr * a.B) << 16) | (uint64_t)(target - g * a.Hq);
+  }
+  int g0 = st->g0, base = st->base;
+  uint64_t res = 0;
+  for (; g0 < n_groups; g0 += 32) {
+    const int g = g0 + lane;
+    bool in_list = false;
+    if (g < n_groups) {
+      const int pr = g / a.B, b = g - pr * a.B;
+      const int q0 = (a.n_pairs - 1 - pr) * kItemRows;
+      const int L = a.key_lens != nullptr ? min(max(a.key_lens[b], 0), a.S) : a.S;
+      const bool busy = sched_tiles(a, q0, L) > 0 || sched_tiles(a, q0 + kBM, L) > 0;
+      in_list = busy != kEmpty;
+    }
+    const uint32_t mask = __ballot_sync(0xffffffffu, in_list);
+    const int cnt = __popc(mask) * a.Hq;
+    if (target < base + cnt) {
+      const int k = (target - base) / a.Hq;
+      const bool mine = in_list && __popc(mask & ((1u << lane) - 1u)) == k;
+      const int gs = g0 + __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+      const int pr = gs / a.B;
+      res = (1ull << 63) | ((uint64_t)(a.n_pairs - 1 - pr) << 32) |
+            ((uint64_t)(gs - pr * a.B) << 16) | (uint64_t)(target - base - k * a.Hq);
+      break;  // later targets are larger: keep this window
+    }
+    base += cnt;
+  }
+  if (lane == 0) {
+    st->g0 = g0;
+    st->base = base;
+  }
+  __syncwarp();
+  return res;
+}
+
+// Unpacks a sched_next result; false when the walk is over.
+__device__ __forceinline__ bool unpack_item(uint64_t v, Item& it) {
+  if (!(v >> 63)) return false;
+  it.q0 = (int)((v >> 32) & 0x7FFFFFFFu) * kItemRows;
+  it.b = (int)((v >> 16) & 0xFFFFu);
+  it.h = (int)(v & 0xFFFFu);
+  return true;
+}
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;
@@ -203,6 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_drain = bar_o + 16;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  SchedArgs* sched = reinterpret_cast<SchedArgs*>(smem + C::kOffSched);
+  // walk[0]: this warp's list of work items, walk[1]: its list of empty items
+  WalkState* walk = reinterpret_cast<WalkState*>(smem + C::kOffWalk) + 2 * (threadIdx.x >> 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int off = p.S - p.T;
@@ -223,7 +265,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    sched->key_lens = p.key_lens;
+    sched->n_pairs = p.n_pairs;
+    sched->B = p.B;
+    sched->Hq = p.Hq;
+    sched->T = p.T;
+    sched->S = p.S;
+    sched->causal = p.causal;
+    sched->all_busy = p.key_lens == nullptr && (!p.causal || p.T <= p.S);
   }
+  if (lane == 0) walk[0] = walk[1] = WalkState{0, 0, 0, 0};
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
@@ -247,9 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool w = mbar_wait(bar, parity, 1, abort_flag);
       return __all_sync(0xffffffffu, w);
     };
-    ItemIter<false> iter;
-    Item it;
-    while (ok && iter.next(p, it)) {
+        Item it;
+    while (ok && unpack_item(sched_next<false>(sched, walk), it)) {
       const int L = key_bound(p, it.b);
       const int n0 = tile_count(p, it.q0, L), n1 = tile_count(p, it.q0 + kBM, L);
       const int nm = max(n0, n1);
@@ -334,9 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       idesc_pv, (acc || kk > 0) ? 1u : 0u);
       }
     };
-    ItemIter<false> iter;
-    Item it;
-    while (ok && iter.next(p, it)) {
+        Item it;
+    while (ok && unpack_item(sched_next<false>(sched, walk), it)) {
       const int L = key_bound(p, it.b);
       const int n0 = tile_count(p, it.q0, L), n1 = tile_count(p, it.q0 + kBM, L);
       const int nm = max(n0, n1);
@@ -415,9 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ns = 0, no = 0;                  // s_full / o_full waits so far
     bool ok = true;
 
-    ItemIter<false> iter;
-    Item it;
-    while (ok && iter.next(p, it)) {
+        Item it;
+    while (ok && unpack_item(sched_next<false>(sched, walk), it)) {
       const int L = key_bound(p, it.b);
       const int q0t = it.q0 + t * kBM;
       const int n = tile_count(p, q0t, L);
@@ -542,24 +590,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (__any_sync(0xffffffffu, has)) {
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t orr[32];
-          tmem_ld32(to + 32 * c, orr);
+        for (int c = 0; c < D / 64; ++c) {
+          uint32_t orr[64];
+          tmem_ld32(to + 64 * c, orr);
+          tmem_ld32(to + 64 * c + 32, orr + 32);
           tmem_wait_ld32(orr);
-          if (i < p.T) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+          tmem_wait_ld32(orr + 32);
+          uint32_t pkd[32];
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 u;
-              u.x = pack_bf16x2(__uint_as_float(orr[8 * v + 0]) * inv,
-                                __uint_as_float(orr[8 * v + 1]) * inv);
-              u.y = pack_bf16x2(__uint_as_float(orr[8 * v + 2]) * inv,
-                                __uint_as_float(orr[8 * v + 3]) * inv);
-              u.z = pack_bf16x2(__uint_as_float(orr[8 * v + 4]) * inv,
-                                __uint_as_float(orr[8 * v + 5]) * inv);
-              u.w = pack_bf16x2(__uint_as_float(orr[8 * v + 6]) * inv,
-                                __uint_as_float(orr[8 * v + 7]) * inv);
-              dst[v] = u;
+          for (int e = 0; e < 32; ++e)
+            pkd[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv,
+                                 __uint_as_float(orr[2 * e + 1]) * inv);
+          if (i < p.T) {
+            __nv_bfloat16* dst = orow + 64 * c;
+            if (p.o_align32) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v) st_global_v8(dst + 16 * v, pkd + 8 * v);
+            } else {
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                reinterpret_cast<uint4*>(dst)[v] =
+                    make_uint4(pkd[4 * v], pkd[4 * v + 1], pkd[4 * v + 2], pkd[4 * v + 3]);
             }
           }
         }
@@ -574,8 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     // Items with no key tile: every row is padded (or past T): O = 0, LSE = -inf.
-    ItemIter<true> empty;
-    while (ok && empty.next(p, it)) {
+    while (ok && unpack_item(sched_next<true>(sched, walk + 1), it)) {
       const int i = it.q0 + t * kBM + r;
       if (i >= p.T) continue;
       const size_t row = ((size_t)it.b * p.Hq + it.h) * p.T + i;

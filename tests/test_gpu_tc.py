@@ -83,3 +83,18 @@ def test_output_buffer_and_no_lse(E):
     torch.cuda.synchronize()
     ro, rl = oracle_fwd(x["q"], x["k"], x["v"], True, None, 1 / 8)
     compare(o, None, ro, rl, torch.bfloat16, "preallocated o")
+
+
+def test_output_view_16_byte_aligned(E):
+    """An output view that starts 16 bytes (not 32) into its allocation takes
+    the 128-bit store path of the epilogue; results must not change."""
+    x = workloads.prefill_inputs(2, 2, 2, 300, 300, 128, "bf16", seed=4, device="cuda")
+    n = x["q"].numel()
+    buf = torch.full((n + 8,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o = buf[8:].view(x["q"].shape)
+    assert o.data_ptr() % 32 == 16
+    E.attn_fwd(x["q"], x["k"], x["v"], o=o, causal=True, return_lse=False)
+    torch.cuda.synchronize()
+    ro, rl = oracle_fwd(x["q"], x["k"], x["v"], True, None, 1 / math.sqrt(128))
+    compare(o, None, ro, rl, torch.bfloat16, "16-byte aligned o")
+    assert torch.isnan(buf[:8].float()).all()
