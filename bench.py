@@ -196,14 +196,14 @@ def decode_flops(Hq, D, kv_lens):
     return 4.0 * Hq * D * float(sum(int(x) for x in kv_lens))
 
 
-def build_case(wid, device):
+def build_case(wid, device, batch=None):
     """Device tensors for one step of workload `wid` and its bookkeeping."""
     import torch
     import workloads
-    w = workloads.WORKLOADS[wid]
+    w = workloads.workload(wid, batch)
     case = {"w": w, "wid": wid}
     if w.kind == "prefill":
-        x = workloads.workload_inputs(wid, device=device)
+        x = workloads.workload_inputs(wid, device=device, batch=batch)
         case.update(x)
         case["o"] = torch.empty_like(x["q"])
         case["lse"] = torch.empty(w.B, w.Hq, w.T, device=device, dtype=torch.float32)
@@ -235,7 +235,7 @@ def build_case(wid, device):
             case["dec_bytes"] = decode_bytes(w.Hkv, w.D, kv)
             case["flops"] += decode_flops(w.Hq, w.D, kv)
     else:
-        d = workloads.workload_inputs(wid, device=device)
+        d = workloads.workload_inputs(wid, device=device, batch=batch)
         case.update(d)
         case["o"] = torch.empty_like(d["q"])
         case["lse"] = torch.empty(w.B, w.Hq, device=device, dtype=torch.float32)
@@ -415,7 +415,7 @@ def bench_ours(args):
     import exact_tiled_attention_49_b300 as E
     E.load()
     peaks = load_peaks()
-    c = build_case(args.workload, device)
+    c = build_case(args.workload, device, args.batch)
     w = c["w"]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     for _ in range(args.warmup):
@@ -564,6 +564,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="smaller batch of the same workload (ncu profiling cases only)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -28,7 +28,7 @@ on the CPU and CUDA generators, so a test draws on one device and copies.
 """
 from __future__ import annotations
 
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 
 import numpy as np
 import torch
@@ -122,9 +122,18 @@ def decode_inputs(B, Hq, Hkv, D, lo, hi, dtype="bf16", seed=0, device="cpu",
             "cache_len": cache_len, "kv_len": cache_len + 1, "S_max": s_max}
 
 
-def workload_inputs(wid: int, device="cpu"):
-    """Inputs of one of the five named workloads, seeded with its id."""
+def workload(wid: int, batch: int | None = None) -> Workload:
+    """Workload `wid`, optionally with a smaller batch (a profiling case: the
+    same shapes per sequence, fewer sequences)."""
     w = WORKLOADS[wid]
+    if batch is None or batch == w.B:
+        return w
+    return replace(w, B=int(batch), name=f"{w.name} [profiling case: B={int(batch)}]")
+
+
+def workload_inputs(wid: int, device="cpu", batch: int | None = None):
+    """Inputs of one of the five named workloads, seeded with its id."""
+    w = workload(wid, batch)
     if wid == 1:
         rs = np.random.RandomState(0)
         Q = rs.randn(w.T, w.D).astype(np.float32)
