@@ -56,6 +56,39 @@ def load_peaks():
                 "source": "fallback"}
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) of
+# each workload's dominant kernel, from the ncu captures summarised under
+# profiles/, keyed by workload id.  Each entry records the sha256 prefix of
+# the kernel source it was measured on; when the source has changed since,
+# the figure no longer describes the kernel and the bench reports null.
+# "scale" converts the captured launch to a full launch of the bench
+# workload by the units it processes (1.0 when captured at full size).
+PROFILED_TRAFFIC = {
+    4: {"source": "exact_tiled_attention_49_b300/csrc/decode.cuh", "sha256": "b95870e96e87",
+        "bytes": 360.429568e6 + 6.840064e6, "scale": 1333948416.0 / 358866944.0,
+        "capture": "decode_split_mma_kernel, profiling case B=16 of workload 4, scaled by "
+                   "the algorithmic K/V bytes (full / captured)"},
+}
+
+
+def source_sha(rel):
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return ""
+
+
+def profiled_traffic(wid):
+    """Measured DRAM bytes per launch of workload `wid`'s dominant kernel, or
+    None when there is no capture of the kernel as it stands."""
+    e = PROFILED_TRAFFIC.get(wid)
+    if e is None or not source_sha(e["source"]).startswith(e["sha256"]):
+        return None
+    return e["bytes"] * e["scale"]
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -298,6 +331,81 @@ def capture_graphs(E, c):
     return graphs, E.attn_kernel_launches() - n0
 
 
+def time_graphs(E, c, steps, flush, clk=None, sync=None):
+    """Warm replays, then `steps` timed replays of the captured kernel groups
+    with the L2 flushed before each step (outside the events).  `sync` (the
+    cross-rank barrier) runs right before and after the timed steps, each
+    time next to a device synchronize.  Returns (per-step ms list, mean ms
+    per group, library launches per step)."""
+    import torch
+    graphs, launches_per_step = capture_graphs(E, c)
+    for _ in range(2):                        # warm replays of the captured step
+        flush.zero_()
+        for _, g in graphs:
+            g.replay()
+    torch.cuda.synchronize()
+    # events[s] = [start, end of group 0, end of group 1, ...]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
+              for _ in range(steps)]
+    if sync is not None:
+        sync()
+    torch.cuda.synchronize()
+    if clk is not None:
+        clk.__enter__()
+    try:
+        for s in range(steps):
+            flush.zero_()                     # L2 flush, outside the timed events
+            events[s][0].record()
+            for i, (_, g) in enumerate(graphs):
+                g.replay()
+                events[s][i + 1].record()
+        torch.cuda.synchronize()
+    finally:
+        if clk is not None:
+            clk.__exit__(None, None, None)
+    if sync is not None:
+        sync()
+    step_ms = [ev[0].elapsed_time(ev[-1]) for ev in events]
+    kern_ms = {name: sum(ev[i].elapsed_time(ev[i + 1]) for ev in events) / steps
+               for i, (name, _) in enumerate(graphs)}
+    return step_ms, kern_ms, launches_per_step
+
+
+def other_workloads(E, skip, device, steps, peaks):
+    """The other benchmark workloads, timed the same way (one entry each):
+    the compute-bound prefills and the HBM-bound decode behind the metric."""
+    import torch
+    out = {}
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    for wid in (3, 4, 5):
+        if wid == skip:
+            continue
+        c = build_case(wid, device)
+        w = c["w"]
+        for _ in range(3):
+            flush.zero_()
+            run_step(E, c)
+        torch.cuda.synchronize()
+        _, kern_ms, _ = time_graphs(E, c, steps, flush)
+        if w.kind == "prefill":
+            v = c["flops"] / (kern_ms["prefill"] * 1e-3) / 1e12
+            out[str(wid)] = {"workload": w.name, "value": v, "unit": "TFLOPS",
+                             "ms": kern_ms["prefill"], "kernel": "fwd_bf16_tc_kernel",
+                             "frac": v / peaks["bf16_tflops"],
+                             "traffic": profiled_traffic(wid)}
+        else:
+            v = c["dec_bytes"] / (kern_ms["decode"] * 1e-3) / 1e9
+            out[str(wid)] = {"workload": w.name, "value": v, "unit": "GB/s",
+                             "ms": kern_ms["decode"],
+                             "kernel": "decode_split_mma_kernel+decode_combine_kernel",
+                             "frac": v / peaks["hbm_gbs"], "traffic": profiled_traffic(wid)}
+        del c
+        torch.cuda.empty_cache()
+    if E.attn_device_error(clear=True) != 0:
+        raise RuntimeError("device error while timing the other workloads")
+    return out
+
+
 def run_e2e(E, c, steps, device):
     """Same step through the public API with pinned host buffers: H2D copy of
     the step's inputs, the step, D2H copy of its outputs, all timed."""
@@ -425,33 +533,12 @@ def bench_ours(args):
     if E.attn_device_error(clear=True) != 0:
         raise RuntimeError("device error during warm-up")
 
-    graphs, launches_per_step = capture_graphs(E, c)
-    for _ in range(2):                        # warm replays of the captured step
-        flush.zero_()
-        for _, g in graphs:
-            g.replay()
-    torch.cuda.synchronize()
-    groups = [name for name, _ in graphs]
     K = args.steps
-    # events[s] = [start, end of group 0, end of group 1, ...]
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(graphs) + 1)]
-              for _ in range(K)]
-    barrier(ws)
-    torch.cuda.synchronize()
-    with ClockSampler(device) as clk:
-        for s in range(K):
-            flush.zero_()                     # L2 flush, outside the timed events
-            events[s][0].record()
-            for i, (_, g) in enumerate(graphs):
-                g.replay()
-                events[s][i + 1].record()
-        torch.cuda.synchronize()
-    barrier(ws)
+    clk = ClockSampler(device)
+    step_ms, kern_ms, launches_per_step = time_graphs(E, c, K, flush, clk,
+                                                      sync=lambda: barrier(ws))
     launches = launches_per_step * K
-    step_ms = [ev[0].elapsed_time(ev[-1]) for ev in events]
     total_ms = reduce_max(sum(step_ms), ws, device)
-    kern_ms = {g: sum(ev[i].elapsed_time(ev[i + 1]) for ev in events) / K
-               for i, g in enumerate(groups)}
     if E.attn_device_error(clear=True) != 0:
         raise RuntimeError("device error during the timed region")
 
@@ -473,7 +560,8 @@ def bench_ours(args):
         peak = peaks["bf16_tflops"]
         out["roofline"] = {"kernel": "fwd_bf16_tc_kernel", "bound": "tensor",
                            "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                           "frac": achieved / peak, "traffic": None,
+                           "frac": achieved / peak,
+                           "traffic": profiled_traffic(args.workload) if args.batch is None else None,
                            "peak_source": peaks["source"] + " bf16 burst"}
         if "dec" in c:
             gbs = c["dec_bytes"] / (kern_ms["decode"] * 1e-3) / 1e9
@@ -488,7 +576,8 @@ def bench_ours(args):
         achieved = c["dec_bytes"] / (kern_ms["decode"] * 1e-3) / 1e9
         out["roofline"] = {"kernel": "decode_split_kernel+decode_combine_kernel",
                            "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                           "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                           "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                           "traffic": profiled_traffic(args.workload) if args.batch is None else None,
                            "peak_source": peaks["source"] + " HBM copy"}
     cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
            "l2": "flushed between steps (256 MiB write, outside the timed events)",
@@ -513,6 +602,10 @@ def bench_ours(args):
         e2e_val = c["dec_bytes"] * ws / (e2e_ms * 1e-3) / 1e9
     out["e2e"] = {"value": e2e_val, "unit": out["unit"], "ms_per_step": e2e_ms,
                   "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    if not args.no_other_workloads and args.batch is None:
+        out["other_workloads"] = other_workloads(E, args.workload, device,
+                                                 max(3, min(K, 10)), peaks)
 
     if rank == 0 and not args.no_cpu_baseline:
         v, unit, cores, sample = cpu_baseline(args.workload, budget_s=args.cpu_budget)
@@ -564,6 +657,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip timing the other benchmark workloads")
     ap.add_argument("--batch", type=int, default=None,
                     help="smaller batch of the same workload (ncu profiling cases only)")
     args = ap.parse_args(argv)
