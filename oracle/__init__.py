@@ -53,7 +53,7 @@ def _load():
     lib = ctypes.CDLL(_SO)
     P = ctypes.c_void_p
     I = ctypes.c_int
-    lib.oracle_attn_fwd.argtypes = [P, P, P, I, I, I, I, I, I, I, I, P,
+    lib.oracle_attn_fwd.argtypes = [P, P, P, I, I, I, I, I, I, I, I, P, P,
                                     ctypes.c_double, P, ctypes.c_int64, P, P, I]
     lib.oracle_attn_fwd.restype = I
     lib.oracle_attn_decode.argtypes = [P, P, P, I, P, I, I, I, I, I,
@@ -87,13 +87,15 @@ def _ptr(a) -> ctypes.c_void_p:
 
 
 def attn_fwd(q, k, v, causal=False, key_lens=None, scale=None, bf16=False,
-             rows=None, nthreads=None):
+             rows=None, nthreads=None, q_pos=None):
     """Prefill forward by the C oracle.
 
     q [B,Hq,T,D], k/v [B,Hkv,S,D].  ``rows`` (optional) is an int64 array of
     flat row ids ``(b*Hq + h)*T + i``; then only those rows are computed and
     the result is packed as o [n,D], lse [n].  Otherwise o [B,Hq,T,D],
-    lse [B,Hq,T].  Returns float64 arrays.
+    lse [B,Hq,T].  ``q_pos`` (optional, [B]) puts query row i of sequence b
+    at key position q_pos[b] + i (chunked prefill against a cache; default
+    S - T, bottom-right).  Returns float64 arrays.
     """
     lib = _load()
     B, Hq, T, D = q.shape
@@ -108,6 +110,11 @@ def attn_fwd(q, k, v, causal=False, key_lens=None, scale=None, bf16=False,
     lens = None
     if key_lens is not None:
         lens = np.ascontiguousarray(key_lens, dtype=np.int32)
+    qp = None
+    if q_pos is not None:
+        qp = np.ascontiguousarray(q_pos, dtype=np.int32)
+        if qp.shape != (B,):
+            raise ValueError("q_pos must have one entry per sequence")
     if rows is not None:
         rows = np.ascontiguousarray(rows, dtype=np.int64)
         n = rows.shape[0]
@@ -118,7 +125,7 @@ def attn_fwd(q, k, v, causal=False, key_lens=None, scale=None, bf16=False,
         o = np.empty((B, Hq, T, D))
         lse = np.empty((B, Hq, T))
     rc = lib.oracle_attn_fwd(_ptr(qa), _ptr(ka), _ptr(va), dt, B, Hq, Hkv, T,
-                             S, D, int(bool(causal)), _ptr(lens),
+                             S, D, int(bool(causal)), _ptr(lens), _ptr(qp),
                              float(scale), _ptr(rows), n, _ptr(o), _ptr(lse),
                              nthreads or default_threads())
     if rc != 0:

@@ -38,6 +38,13 @@
  *  - GQA grouping is contiguous: query head h reads KV head h / (Hq / Hkv).
  *  - LSE is the natural log of sum_j exp(s_j), s_j already scaled.
  *
+ * Chunked prefill against a KV cache ("Implementing attention from
+ * scratch", KV caching: new queries sit after the cached positions, so
+ * their offset is the cache length plus the position within the chunk):
+ * with q_pos[b] given, query row i of sequence b sits at key position
+ * q_pos[b] + i instead of i + S - T; visibility and padded rows follow from
+ * that position as above.
+ *
  * Inputs may be float64, float32 or bfloat16 (raw 16-bit patterns); every
  * element is widened exactly to double before use.  Layouts (contiguous):
  *   prefill  q [B,Hq,T,D], k/v [B,Hkv,S,D], o [.., D] float64, lse float64
@@ -121,6 +128,7 @@ typedef struct {
   const void *q, *k, *v;
   int dtype, B, Hq, Hkv, T, S, D, causal, decode;
   const int32_t* lens; /* key_lens (prefill) or kv_lens (decode); may be NULL */
+  const int32_t* q_pos; /* prefill: key position of query row 0 per sequence; may be NULL */
   double scale;
   /* which rows: NULL = all, else flat row ids (b*Hq + h)*T + i */
   const int64_t* rows;
@@ -148,7 +156,9 @@ static void* run_rows(void* arg) {
     int b = (int)(bh / jb->Hq);
     int g = h / G;
     int L = jb->lens ? jb->lens[b] : jb->S;
-    int64_t row_pos = jb->decode ? (int64_t)L - 1 : i + (jb->S - jb->T);
+    int64_t row_pos = jb->decode  ? (int64_t)L - 1
+                      : jb->q_pos ? (int64_t)jb->q_pos[b] + i
+                                  : i + (jb->S - jb->T);
     int64_t q_off = flat * jb->D;
     int64_t kv_off = ((int64_t)b * jb->Hkv + g) * (int64_t)jb->S * jb->D;
     attention_row(jb->q, q_off, jb->k, kv_off, jb->v, kv_off, jb->dtype,
@@ -195,10 +205,12 @@ static int check_shape(int B, int Hq, int Hkv, int T, int S, int D) {
 
 /* Prefill forward.  rows == NULL computes every row (o is [B,Hq,T,D],
  * lse [B,Hq,T]); otherwise only the n_rows listed flat row ids, packed
- * (o is [n_rows,D], lse [n_rows]).  Returns 0 on success. */
+ * (o is [n_rows,D], lse [n_rows]).  q_pos (may be NULL) places query row 0
+ * of sequence b at key position q_pos[b] (chunked prefill against a
+ * cache); NULL means bottom-right, S - T.  Returns 0 on success. */
 int oracle_attn_fwd(const void* q, const void* k, const void* v, int dtype,
                     int B, int Hq, int Hkv, int T, int S, int D, int causal,
-                    const int32_t* key_lens, double scale,
+                    const int32_t* key_lens, const int32_t* q_pos, double scale,
                     const int64_t* rows, int64_t n_rows, double* o,
                     double* lse, int nthreads) {
   if (check_shape(B, Hq, Hkv, T, S, D)) return 1;
@@ -210,8 +222,8 @@ int oracle_attn_fwd(const void* q, const void* k, const void* v, int dtype,
   memset(&jb, 0, sizeof jb);
   jb.q = q; jb.k = k; jb.v = v; jb.dtype = dtype;
   jb.B = B; jb.Hq = Hq; jb.Hkv = Hkv; jb.T = T; jb.S = S; jb.D = D;
-  jb.causal = causal; jb.decode = 0; jb.lens = key_lens; jb.scale = scale;
-  jb.rows = rows; jb.o = o; jb.lse = lse;
+  jb.causal = causal; jb.decode = 0; jb.lens = key_lens; jb.q_pos = q_pos;
+  jb.scale = scale; jb.rows = rows; jb.o = o; jb.lse = lse;
   int64_t total = rows ? n_rows : (int64_t)B * Hq * T;
   if (rows)
     for (int64_t r = 0; r < n_rows; ++r)

@@ -38,28 +38,36 @@ def _as_f64(x: np.ndarray, bf16: bool) -> np.ndarray:
     return np.asarray(x, dtype=np.float64)
 
 
-def visibility(T: int, S: int, L: int, causal: bool) -> tuple[np.ndarray, np.ndarray]:
+def visibility(T: int, S: int, L: int, causal: bool,
+               q0: int | None = None) -> tuple[np.ndarray, np.ndarray]:
     """(row_valid [T], visible [T,S]) for one sequence.
 
-    Query row i sits at key position i + S - T (bottom-right alignment).  It is
-    a padded row when that position is >= L.  Key j is visible to row i when
-    j < L and, for causal attention, j <= i + S - T.
+    Query row i sits at key position q0 + i, where q0 = S - T by default
+    (bottom-right alignment) or the cache length before the chunk (chunked
+    prefill against a cache).  It is a padded row when that position is
+    >= L.  Key j is visible to row i when j < L and, for causal attention,
+    j <= q0 + i.
     """
-    pos = np.arange(T)[:, None] + (S - T)
+    if q0 is None:
+        q0 = S - T
+    pos = np.arange(T)[:, None] + q0
     j = np.arange(S)[None, :]
     vis = j < L
     if causal:
         vis = vis & (j <= pos)
-    row_valid = (np.arange(T) + (S - T)) < L
+    row_valid = (np.arange(T) + q0) < L
     vis = vis & row_valid[:, None]
     return row_valid, vis
 
 
-def attn_fwd_np(q, k, v, causal=False, key_lens=None, scale=None, bf16=False):
+def attn_fwd_np(q, k, v, causal=False, key_lens=None, scale=None, bf16=False,
+                q_pos=None):
     """Full-softmax attention in float64.  q [B,Hq,T,D], k/v [B,Hkv,S,D].
 
-    Returns (o [B,Hq,T,D], lse [B,Hq,T]); rows with no visible key (padded
-    rows included) are O = 0, LSE = -inf.
+    ``q_pos`` ([B], optional) puts query row i of sequence b at key position
+    q_pos[b] + i (chunked prefill); default S - T.  Returns (o [B,Hq,T,D],
+    lse [B,Hq,T]); rows with no visible key (padded rows included) are O = 0,
+    LSE = -inf.
     """
     q, k, v = (_as_f64(x, bf16) for x in (q, k, v))
     B, Hq, T, D = q.shape
@@ -72,17 +80,20 @@ def attn_fwd_np(q, k, v, causal=False, key_lens=None, scale=None, bf16=False):
     lse = np.full((B, Hq, T), _NEG_INF)
     for b in range(B):
         L = S if key_lens is None else int(key_lens[b])
-        _, vis = visibility(T, S, L, causal)
+        _, vis = visibility(T, S, L, causal, None if q_pos is None else int(q_pos[b]))
+        # Masked-out scores are never formed: a key row outside the visible
+        # set may hold anything (even NaN) without touching the result.
         has = vis.any(axis=1)
         for h in range(Hq):
             g = h // G
-            s = (q[b, h] @ k[b, g].T) * scale
+            with np.errstate(invalid="ignore"):
+                s = (q[b, h] @ np.where(vis.any(axis=0)[:, None], k[b, g], 0.0).T) * scale
             s = np.where(vis, s, _NEG_INF)
             m = np.where(has, s.max(axis=1), 0.0)
             e = np.where(vis, np.exp(s - m[:, None]), 0.0)
             z = e.sum(axis=1)
             zs = np.where(has, z, 1.0)
-            o[b, h] = (e / zs[:, None]) @ v[b, g]
+            o[b, h] = (e / zs[:, None]) @ np.where(vis.any(axis=0)[:, None], v[b, g], 0.0)
             lse[b, h] = np.where(has, m + np.log(zs), _NEG_INF)
     return o, lse
 
