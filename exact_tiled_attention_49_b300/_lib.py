@@ -23,6 +23,8 @@ ATTN_F32, ATTN_BF16 = 0, 1
 _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
 SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _F, _P]),
+    "attn_fwd_chunked": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
+                              _P]),
     "attn_decode_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
                          ctypes.c_size_t, _P]),
@@ -139,6 +141,48 @@ def attn_fwd(q, k, v, o=None, lse=None, causal=False, key_lens=None, scale=None,
     rc = lib.attn_fwd(*ptrs, lp, B, Hq, Hkv, T, S, D, dt, int(bool(causal)), kl,
                       float(scale), _stream(stream))
     _check(rc, "attn_fwd")
+    return o, lse
+
+
+def attn_fwd_chunked(q, kcache, vcache, q_pos, kv_lens, o=None, lse=None, causal=True,
+                     scale=None, return_lse=True, stream=None):
+    """Chunked prefill against a KV cache.  q [B,Hq,T,D], caches
+    [B,Hkv,S_max,D] (holding the chunk's own K/V rows), q_pos and kv_lens
+    int32 CUDA [B]: query row i of sequence b sits at key position
+    q_pos[b] + i and sees keys below kv_lens[b] (causally, up to itself).
+
+    Returns (o, lse) like attn_fwd.
+    """
+    lib = load()
+    B, Hq, T, D = q.shape
+    Bk, Hkv, S_max, Dk = kcache.shape
+    if Bk != B or Dk != D or tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError("q/cache shape mismatch")
+    if kcache.dtype != q.dtype or vcache.dtype != q.dtype:
+        raise TypeError("q and the caches must share one dtype")
+    dt = _dtype_code(q)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, T), device=q.device, dtype=torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    ptrs = [_dev(q, "q", ndim=4), _dev(kcache, "kcache", ndim=4),
+            _dev(vcache, "vcache", ndim=4), _dev(o, "o", dtype=q.dtype, ndim=4)]
+    if tuple(o.shape) != tuple(q.shape):
+        raise ValueError("o must have q's shape")
+    lp = None
+    if lse is not None:
+        lp = _dev(lse, "lse", dtype=torch.float32)
+        if lse.numel() != B * Hq * T:
+            raise ValueError("lse must hold B*Hq*T floats")
+    qp = _dev(q_pos, "q_pos", dtype=torch.int32, ndim=1)
+    kl = _dev(kv_lens, "kv_lens", dtype=torch.int32, ndim=1)
+    if q_pos.numel() != B or kv_lens.numel() != B:
+        raise ValueError("q_pos and kv_lens must have B entries")
+    rc = lib.attn_fwd_chunked(*ptrs, lp, qp, kl, B, Hq, Hkv, T, S_max, D, dt,
+                              int(bool(causal)), float(scale), _stream(stream))
+    _check(rc, "attn_fwd_chunked")
     return o, lse
 
 

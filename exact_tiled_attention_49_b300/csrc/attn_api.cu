@@ -143,7 +143,7 @@ int launch_status() {
 template <int D>
 int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                   int Hq, int Hkv, int T, int S, int causal, const int32_t* key_lens,
-                  float scale, cudaStream_t st) {
+                  const int32_t* q_pos, float scale, cudaStream_t st) {
   using namespace attn::tcfwd;
   static std::atomic<uint64_t> smem_done{0};
   auto kernel = fwd_bf16_tc_kernel<D>;
@@ -157,6 +157,7 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* l
   p.o = o;
   p.lse = lse;
   p.key_lens = key_lens;
+  p.q_pos = q_pos;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -178,7 +179,7 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* l
 template <int NC>
 int launch_fwd_f32(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                    int Hq, int Hkv, int T, int S, int D, int causal, const int32_t* key_lens,
-                   float scale, cudaStream_t st) {
+                   const int32_t* q_pos, float scale, cudaStream_t st) {
   using namespace attn::f32fwd;
   static std::atomic<uint64_t> smem_done{0};
   auto kernel = fwd_f32_kernel<NC>;
@@ -191,6 +192,7 @@ int launch_fwd_f32(const void* q, const void* k, const void* v, void* o, float* 
   p.o = static_cast<float*>(o);
   p.lse = lse;
   p.key_lens = key_lens;
+  p.q_pos = q_pos;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -253,33 +255,37 @@ int launch_decode_d(const attn::decode::Params& p, int G, cudaStream_t st) {
 
 bool finite_positive(float x) { return std::isfinite(x) && x > 0.f; }
 
-}  // namespace
-
-extern "C" {
-
-int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
-             int Hkv, int T, int S, int D, int dtype, int causal, const int32_t* key_lens,
-             float scale, attn_stream_t stream) {
+// Shared by attn_fwd and attn_fwd_chunked: validation and kernel choice.
+int fwd_dispatch(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                 int Hq, int Hkv, int T, int S, int D, int dtype, int causal,
+                 const int32_t* key_lens, const int32_t* q_pos, float scale,
+                 attn_stream_t stream) {
   if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || S <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0 || !finite_positive(scale)) return ATTN_ERR_INVALID_ARG;
   if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
   if (lse != nullptr && !aligned4(lse)) return ATTN_ERR_INVALID_ARG;
   if (key_lens != nullptr && !aligned4(key_lens)) return ATTN_ERR_INVALID_ARG;
+  if (q_pos != nullptr && !aligned4(q_pos)) return ATTN_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == ATTN_BF16) {
     if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
       return ATTN_ERR_INVALID_ARG;
-    if (D == 64) return launch_fwd_tc<64>(q, k, v, o, lse, B, Hq, Hkv, T, S, causal, key_lens, scale, st);
-    return launch_fwd_tc<128>(q, k, v, o, lse, B, Hq, Hkv, T, S, causal, key_lens, scale, st);
+    if (D == 64)
+      return launch_fwd_tc<64>(q, k, v, o, lse, B, Hq, Hkv, T, S, causal, key_lens, q_pos, scale,
+                               st);
+    return launch_fwd_tc<128>(q, k, v, o, lse, B, Hq, Hkv, T, S, causal, key_lens, q_pos, scale,
+                              st);
   }
   if (dtype == ATTN_F32) {
     if (D > 256) return ATTN_ERR_UNSUPPORTED;
     if (!aligned4(q) || !aligned4(k) || !aligned4(v) || !aligned4(o)) return ATTN_ERR_INVALID_ARG;
     const int nc = (D + 31) / 32;
-#define ATTN_F32_CASE(N) \
-  case N: return launch_fwd_f32<N>(q, k, v, o, lse, B, Hq, Hkv, T, S, D, causal, key_lens, scale, st);
+#define ATTN_F32_CASE(N)                                                                    \
+  case N:                                                                                   \
+    return launch_fwd_f32<N>(q, k, v, o, lse, B, Hq, Hkv, T, S, D, causal, key_lens, q_pos, \
+                             scale, st);
     switch (nc) {
       ATTN_F32_CASE(1) ATTN_F32_CASE(2) ATTN_F32_CASE(3) ATTN_F32_CASE(4)
       ATTN_F32_CASE(5) ATTN_F32_CASE(6) ATTN_F32_CASE(7) ATTN_F32_CASE(8)
@@ -288,6 +294,26 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
 #undef ATTN_F32_CASE
   }
   return ATTN_ERR_INVALID_ARG;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int T, int S, int D, int dtype, int causal, const int32_t* key_lens,
+             float scale, attn_stream_t stream) {
+  return fwd_dispatch(q, k, v, o, lse, B, Hq, Hkv, T, S, D, dtype, causal, key_lens, nullptr,
+                      scale, stream);
+}
+
+int attn_fwd_chunked(const void* q, const void* kcache, const void* vcache, void* o, float* lse,
+                     const int32_t* q_pos, const int32_t* kv_lens, int B, int Hq, int Hkv,
+                     int T, int S_max, int D, int dtype, int causal, float scale,
+                     attn_stream_t stream) {
+  if (!q_pos || !kv_lens) return ATTN_ERR_INVALID_ARG;
+  return fwd_dispatch(q, kcache, vcache, o, lse, B, Hq, Hkv, T, S_max, D, dtype, causal, kv_lens,
+                      q_pos, scale, stream);
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int S_max, int D) {

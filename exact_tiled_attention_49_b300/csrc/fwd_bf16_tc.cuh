@@ -66,8 +66,8 @@ struct Cfg {
   static constexpr uint32_t kOffSlots = kQTiles * kQBytes;
   static constexpr uint32_t kOffBars = kOffSlots + kSlots * kTileBytes;
   // barriers: q_full[2], q_empty[2], slot_full[S], slot_empty[S], s_full[2],
-  // p_half[2][2], o_full[2], drain
-  static constexpr int kNumBars = 2 + 2 + 2 * kSlots + 2 + 4 + 2 + 1;
+  // p_half[2][2], o_full[2], drain, tail
+  static constexpr int kNumBars = 2 + 2 + 2 * kSlots + 2 + 4 + 2 + 1 + 1;
   static constexpr uint32_t kOffMisc = kOffBars + 8 * kNumBars;    // TMEM address, abort flag
   static constexpr uint32_t kOffSched = (kOffMisc + 16 + 15) / 16 * 16;  // SchedArgs
   static constexpr uint32_t kOffWalk = kOffSched + 48;                   // WalkState[warps][2]
@@ -81,6 +81,7 @@ struct Params {
   void* o;                  // [B,Hq,T,D] bf16
   float* lse;               // [B,Hq,T] or null
   const int32_t* key_lens;  // [B] or null
+  const int32_t* q_pos;     // [B] key position of query row 0, or null (S - T)
   int B, Hq, Hkv, T, S;
   int causal;
   int n_pairs;              // ceil(T / 256)
@@ -98,12 +99,20 @@ __device__ __forceinline__ int key_bound(const Params& p, int b) {
   return p.key_lens != nullptr ? min(max(p.key_lens[b], 0), p.S) : p.S;
 }
 
+// Key position of query row 0 of sequence b: S - T (bottom-right) or, for
+// chunked prefill against a cache, q_pos[b].  Clamping to [-(T + 256), S]
+// keeps the index arithmetic in range and changes nothing: below it every
+// row's position is negative, above it every row is padded.
+__device__ __forceinline__ int q_offset(const int32_t* q_pos, int b, int T, int S) {
+  return q_pos != nullptr ? min(max(q_pos[b], -(T + 256)), S) : S - T;
+}
+
 // Number of key tiles the query tile starting at row q0 must visit (0 when
-// every row of the tile is past T, padded, or sees no key).  Every role
-// computes it the same way so they agree on the trip counts.
-__device__ __forceinline__ int tile_count(const Params& p, int q0, int L) {
+// every row of the tile is past T, padded, or sees no key); `off` is the
+// sequence's q_offset.  Every role computes it the same way so they agree
+// on the trip counts.
+__device__ __forceinline__ int tile_count(const Params& p, int q0, int L, int off) {
   if (q0 >= p.T) return 0;
-  const int off = p.S - p.T;
   if (q0 + off >= L) return 0;  // every row of the tile is a padded row
   int kv_end = L;
   if (p.causal) kv_end = min(L, q0 + kBM + off);  // last row sees keys <= q0+BM-1+off
@@ -118,6 +127,7 @@ __device__ __forceinline__ int tile_count(const Params& p, int q0, int L) {
 // parameter read in the kernel would become a slow local load.
 struct SchedArgs {
   const int32_t* key_lens;
+  const int32_t* q_pos;
   int n_pairs, B, Hq, T, S, causal, all_busy;
 };
 struct WalkState {
@@ -128,9 +138,9 @@ struct WalkState {
 };
 
 // Key tiles of the query tile starting at q0 (the rule of tile_count).
-__device__ __forceinline__ int sched_tiles(const SchedArgs& a, int q0, int L) {
-  if (q0 >= a.T || q0 + a.S - a.T >= L) return 0;
-  const int kv_end = a.causal ? min(L, q0 + kBM + a.S - a.T) : L;
+__device__ __forceinline__ int sched_tiles(const SchedArgs& a, int q0, int L, int off) {
+  if (q0 >= a.T || q0 + off >= L) return 0;
+  const int kv_end = a.causal ? min(L, q0 + kBM + off) : L;
   return kv_end <= 0 ? 0 : (kv_end + kBN - 1) / kBN;
 }
 
@@ -180,7 +190,8 @@ __device__ __noinline__ uint64_t sched_next(const SchedArgs* args, WalkState* st
       const int pr = g / a.B, b = g - pr * a.B;
       const int q0 = (a.n_pairs - 1 - pr) * kItemRows;
       const int L = a.key_lens != nullptr ? min(max(a.key_lens[b], 0), a.S) : a.S;
-      const bool busy = sched_tiles(a, q0, L) > 0 || sched_tiles(a, q0 + kBM, L) > 0;
+      const int off = q_offset(a.q_pos, b, a.T, a.S);
+      const bool busy = sched_tiles(a, q0, L, off) > 0 || sched_tiles(a, q0 + kBM, L, off) > 0;
       in_list = busy != kEmpty;
     }
     const uint32_t mask = __ballot_sync(0xffffffffu, in_list);
@@ -213,6 +224,19 @@ __device__ __forceinline__ bool unpack_item(uint64_t v, Item& it) {
   return true;
 }
 
+// Zero rows [r0, kBN) of a K/V slot at shared address `slot` (kChunks
+// 128-byte column chunks of kBN rows each; a whole 128-byte row is zeroed,
+// so the swizzle does not matter), then make the writes visible to the
+// tensor cores.  Whole warp.
+template <int kChunks>
+__device__ __forceinline__ void zero_rows_from(uint32_t slot, int r0, int lane) {
+  for (int idx = r0 * 8 + lane; idx < kBN * 8; idx += 32)
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) st_shared_zero16(slot + c * (kBN * 128) + idx * 16);
+  fence_proxy_async_shared();
+  __syncwarp();
+}
+
 __device__ __forceinline__ float max3f(float a, float b, float c) {
   float r;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -240,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_p = bar_s + 16;                        // p_half[t][h] = bar_p + 16t + 8h
   const uint32_t bar_o = bar_p + 32;                        // o_full[t]
   const uint32_t bar_drain = bar_o + 16;
+  const uint32_t bar_tail = bar_drain + 8;  // producer-private: the V tile that straddles L
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   SchedArgs* sched = reinterpret_cast<SchedArgs*>(smem + C::kOffSched);
@@ -247,7 +272,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   WalkState* walk = reinterpret_cast<WalkState*>(smem + C::kOffWalk) + 2 * (threadIdx.x >> 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int off = p.S - p.T;
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < kQTiles; ++t) {
@@ -263,16 +287,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_empty(s), 1);
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_tail, 1);
     *abort_flag = 0;
     fence_mbar_init();
     sched->key_lens = p.key_lens;
+    sched->q_pos = p.q_pos;
     sched->n_pairs = p.n_pairs;
     sched->B = p.B;
     sched->Hq = p.Hq;
     sched->T = p.T;
     sched->S = p.S;
     sched->causal = p.causal;
-    sched->all_busy = p.key_lens == nullptr && (!p.causal || p.T <= p.S);
+    sched->all_busy =
+        p.key_lens == nullptr && p.q_pos == nullptr && (!p.causal || p.T <= p.S);
   }
   if (lane == 0) walk[0] = walk[1] = WalkState{0, 0, 0, 0};
   if (warp == kMmaWarp) {
@@ -292,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
     }
-    int ring = 0, qi = 0;
+    int ring = 0, qi = 0, ntail = 0;
     bool ok = true;
     auto wait_bar = [&](uint32_t bar, uint32_t parity) {
       const bool w = mbar_wait(bar, parity, 1, abort_flag);
@@ -301,11 +328,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         Item it;
     while (ok && unpack_item(sched_next<false>(sched, walk), it)) {
       const int L = key_bound(p, it.b);
-      const int n0 = tile_count(p, it.q0, L), n1 = tile_count(p, it.q0 + kBM, L);
+      const int off = q_offset(p.q_pos, it.b, p.T, p.S);
+      const int n0 = tile_count(p, it.q0, L, off), n1 = tile_count(p, it.q0 + kBM, L, off);
       const int nm = max(n0, n1);
       if (nm == 0) continue;
       const int bh_q = it.b * p.Hq + it.h;
       const int bh_kv = it.b * p.Hkv + it.h / (p.Hq / p.Hkv);
+      // The V tile that holds key rows at or past L, if L falls inside a
+      // tile below S: those rows get P = 0, but 0 * NaN is NaN, so they are
+      // zeroed before P V can read them (a cache's unused tail may hold
+      // anything; rows past S are zero-filled by TMA already).  That tile
+      // lands on a private barrier; this warp zeroes the rows and then
+      // completes the slot's full barrier itself.
+      const int j_tail = (L < p.S && (L & (kBN - 1)) != 0) ? L / kBN : -1;
       for (int t = 0; t < kQTiles && ok; ++t) {
         if (qi > 0) ok = wait_bar(bar_qempty(t), (qi - 1) & 1);
         if (!ok) break;
@@ -322,13 +357,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int slot = ring % C::kSlots;
         if (ring >= C::kSlots) ok = wait_bar(bar_empty(slot), ((ring / C::kSlots) - 1) & 1);
         if (!ok) break;
+        const uint32_t dst = s_slots + slot * C::kTileBytes;
+        const bool tail = (u & 1) && (u >> 1) == j_tail;
+        const uint32_t bar_land = tail ? bar_tail : bar_full(slot);
         if (lane == 0) {
-          const uint32_t dst = s_slots + slot * C::kTileBytes;
-          mbar_arrive_expect_tx(bar_full(slot), C::kTileBytes);
+          mbar_arrive_expect_tx(bar_land, C::kTileBytes);
           const CUtensorMap* tm = (u & 1) ? &tm_v : &tm_k;
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(dst + c * C::kChunkBytes, tm, bar_full(slot), c * 64, (u >> 1) * kBN,
-                        bh_kv);
+            tma_load_3d(dst + c * C::kChunkBytes, tm, bar_land, c * 64, (u >> 1) * kBN, bh_kv);
+        }
+        if (tail) {
+          ok = wait_bar(bar_tail, ntail & 1);
+          ++ntail;
+          if (!ok) break;
+          zero_rows_from<C::kChunks>(dst, L & (kBN - 1), lane);
+          if (lane == 0) mbar_arrive(bar_full(slot));
         }
         ++ring;
       }
@@ -339,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar_full(u % C::kSlots), (u / C::kSlots) & 1, 3);
     if (qi > 0)
       for (int t = 0; t < kQTiles; ++t) mbar_wait(bar_qfull(t), (qi - 1) & 1, 3);
+    if (ntail > 0) mbar_wait(bar_tail, (ntail - 1) & 1, 3);
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
@@ -387,7 +431,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         Item it;
     while (ok && unpack_item(sched_next<false>(sched, walk), it)) {
       const int L = key_bound(p, it.b);
-      const int n0 = tile_count(p, it.q0, L), n1 = tile_count(p, it.q0 + kBM, L);
+      const int off = q_offset(p.q_pos, it.b, p.T, p.S);
+      const int n0 = tile_count(p, it.q0, L, off), n1 = tile_count(p, it.q0 + kBM, L, off);
       const int nm = max(n0, n1);
       if (nm == 0) continue;
       ok = wait_bar(bar_qfull(0), qi & 1) && wait_bar(bar_qfull(1), qi & 1);
@@ -467,8 +512,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         Item it;
     while (ok && unpack_item(sched_next<false>(sched, walk), it)) {
       const int L = key_bound(p, it.b);
+      const int off = q_offset(p.q_pos, it.b, p.T, p.S);
       const int q0t = it.q0 + t * kBM;
-      const int n = tile_count(p, q0t, L);
+      const int n = tile_count(p, q0t, L, off);
       const int i = q0t + r;
       const int pos = i + off;
       const bool row_ok = (i < p.T) && (pos < L);

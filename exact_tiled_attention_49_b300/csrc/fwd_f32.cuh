@@ -31,6 +31,7 @@ struct Params {
   float* o;
   float* lse;
   const int32_t* key_lens;
+  const int32_t* q_pos;   // [B] key position of query row 0, or null (S - T)
   int B, Hq, Hkv, T, S, D;
   int causal;
   float scale;
@@ -53,7 +54,9 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(Params p) {
   const int h = blockIdx.y, b = blockIdx.z;
   const int g = h / (p.Hq / p.Hkv);
   const int q0 = blockIdx.x * kBM;
-  const int off = p.S - p.T;  // bottom-right alignment: row i sits at key i + off
+  // Row i sits at key position i + off: bottom-right (S - T) or, for chunked
+  // prefill against a cache, q_pos[b] (clamped: see the tcgen05 kernel).
+  const int off = p.q_pos != nullptr ? min(max(p.q_pos[b], -(p.T + 256)), p.S) : p.S - p.T;
   int L = p.S;
   if (p.key_lens != nullptr) L = min(max(p.key_lens[b], 0), p.S);
 
@@ -82,7 +85,9 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(Params p) {
     __syncthreads();
     for (int idx = threadIdx.x; idx < kBN * D; idx += blockDim.x) {
       const int r = idx / D, c = idx - r * D;
-      const bool in = (k0 + r) < p.S;
+      // Rows at or past L are never visible; they load as 0 so that a
+      // cache's unused tail (which may hold anything) cannot reach P V.
+      const bool in = (k0 + r) < L;
       const size_t gi = kv_base + (size_t)(k0 + r) * D + c;
       k_s[r * (D + 1) + c] = in ? p.k[gi] : 0.f;
       v_s[r * D + c] = in ? p.v[gi] : 0.f;

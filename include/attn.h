@@ -99,6 +99,40 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
              attn_stream_t stream);
 
 /*
+ * attn_fwd_chunked -- chunked prefill against a KV cache: a chunk of up to T
+ * new queries per sequence attends over that sequence's cache, which already
+ * holds the chunk's own K/V rows (append them first, e.g. with one copy per
+ * chunk).  "Implementing attention from scratch", KV caching: a new query's
+ * position is the cache length plus its position within the chunk, and the
+ * causal mask is aligned to that position (bottom-right, per sequence).
+ *
+ * Query row i of sequence b sits at key position p = q_pos[b] + i.  With
+ * L = kv_lens[b] (clamped to [0, S_max]):
+ *     key j is visible to row i   iff  j < L and (!causal or j <= p)
+ *     row i is a padded row       iff  p >= L
+ * A chunk shorter than T for sequence b (ragged chunks) is expressed by
+ * kv_lens[b] = q_pos[b] + (its chunk length): rows past it are padded rows.
+ * Padded rows and rows that see no key are written as O = 0, LSE = -inf.
+ * attn_fwd is the special case q_pos[b] = S - T.  Cache rows at or past L
+ * are never used, whatever they hold.
+ *
+ *   q                 [B,Hq,T,D]      dtype          (read)
+ *   kcache, vcache    [B,Hkv,S_max,D] dtype          (read)
+ *   o                 [B,Hq,T,D]      dtype          (written)
+ *   lse               [B,Hq,T]        float32        (written; NULL = do not emit)
+ *   q_pos             [B]             int32, device  (read; any value)
+ *   kv_lens           [B]             int32, device  (read; clamped to [0, S_max])
+ *
+ * Supported sizes, types and alignment as for attn_fwd (S_max in place of
+ * S).  q_pos and kv_lens must not be NULL.  Returns ATTN_OK,
+ * ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA.
+ */
+ATTN_API int attn_fwd_chunked(const void* q, const void* kcache, const void* vcache, void* o,
+                              float* lse, const int32_t* q_pos, const int32_t* kv_lens,
+                              int B, int Hq, int Hkv, int T, int S_max, int D, int dtype,
+                              int causal, float scale, attn_stream_t stream);
+
+/*
  * attn_decode_workspace_size -- bytes of device scratch attn_decode needs for
  * a batch of B sequences, Hq query heads, caches of S_max positions and head
  * size D.  The caller allocates it (any alignment >= 16 bytes) and may reuse

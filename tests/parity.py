@@ -20,13 +20,14 @@ TOL = {
 }
 
 
-def oracle_fwd(q, k, v, causal, key_lens, scale, rows=None):
+def oracle_fwd(q, k, v, causal, key_lens, scale, rows=None, q_pos=None):
     qn, bf = to_numpy_exact(q)
     kn, _ = to_numpy_exact(k)
     vn, _ = to_numpy_exact(v)
     kl = None if key_lens is None else key_lens.cpu().numpy()
+    qp = None if q_pos is None else q_pos.cpu().numpy()
     return oracle.attn_fwd(qn, kn, vn, causal=causal, key_lens=kl, scale=scale,
-                           bf16=bf, rows=rows)
+                           bf16=bf, rows=rows, q_pos=qp)
 
 
 def oracle_decode(q, kc, vc, kv_lens, scale):
