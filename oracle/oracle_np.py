@@ -173,3 +173,66 @@ def attn_tiled_online_np(q, k, v, causal=False, key_lens=None, scale=None,
                 o[b, h, q0:q1] = np.where(has[:, None], acc / ls[:, None], 0.0)
                 lse[b, h, q0:q1] = np.where(has, m + np.log(ls), _NEG_INF)
     return o, lse
+
+
+def attn_bwd_np(q, k, v, do, causal=False, key_lens=None, scale=None, bf16=False,
+                q_pos=None):
+    """Gradients of attention in float64: (dq, dk, dv), plus (o, lse).
+
+    The chain rule through the softmax, written out step by step for each
+    (b, h) with g = h / (Hq / Hkv).  Sources: "Hands-on build guide:
+    FlashAttention-style tiled attention kernel in pure NumPy", Roadmap
+    (gradient through attention: dL/dQ, dL/dK, dL/dV by the chain rule);
+    "Self-Attention: Implementation, Complexity, and Efficient Variants",
+    FlashAttention follow-up (the backward pass recomputes the attention
+    matrix on chip instead of storing it); "Implementing attention from
+    scratch", Testing against a reference (gradient comparisons against a
+    float64 reference).  This function is that reference:
+
+        S  = scale * Q K^T            (visible entries only)
+        P  = softmax_rows(S)          (0 on hidden keys; rows with no
+                                       visible key are all 0)
+        O  = P V
+        dV = P^T dO                   (summed over the Hq/Hkv heads of g)
+        dP = dO V^T
+        Δ  = rowsum(dO * O)           (= rowsum(P * dP))
+        dS = P * (dP - Δ)
+        dQ = scale * dS K
+        dK = scale * dS^T Q           (summed over the heads of g)
+
+    q, do [B,Hq,T,D]; k, v [B,Hkv,S,D]; masks and q_pos as in attn_fwd_np.
+    """
+    q, k, v, do = (_as_f64(x, bf16) for x in (q, k, v, do))
+    B, Hq, T, D = q.shape
+    _, Hkv, S, _ = k.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    G = Hq // Hkv
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    o = np.zeros_like(q)
+    lse = np.full((B, Hq, T), _NEG_INF)
+    for b in range(B):
+        L = S if key_lens is None else int(key_lens[b])
+        _, vis = visibility(T, S, L, causal, None if q_pos is None else int(q_pos[b]))
+        has = vis.any(axis=1)
+        keys = vis.any(axis=0)
+        for h in range(Hq):
+            g = h // G
+            kg = np.where(keys[:, None], k[b, g], 0.0)
+            vg = np.where(keys[:, None], v[b, g], 0.0)
+            s = np.where(vis, (q[b, h] @ kg.T) * scale, _NEG_INF)
+            m = np.where(has, s.max(axis=1), 0.0)
+            e = np.where(vis, np.exp(s - m[:, None]), 0.0)
+            z = np.where(has, e.sum(axis=1), 1.0)
+            p = e / z[:, None]
+            o[b, h] = p @ vg
+            lse[b, h] = np.where(has, m + np.log(z), _NEG_INF)
+            dv[b, g] += p.T @ do[b, h]
+            dp = do[b, h] @ vg.T
+            delta = (do[b, h] * o[b, h]).sum(axis=1)
+            ds = p * (dp - delta[:, None])
+            dq[b, h] = scale * (ds @ kg)
+            dk[b, g] += scale * (ds.T @ q[b, h])
+    return dq, dk, dv, o, lse
