@@ -12,12 +12,13 @@ from ._lib import (ATTN_BF16, ATTN_ERR_CUDA, ATTN_ERR_INVALID_ARG,  # noqa: F401
                    ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_F32, ATTN_OK,
                    LIB_PATH, NOALLOC_SCRATCH_BYTES, SIGNATURES, AttnError, attn_decode,
                    attn_decode_noalloc,
+                   attn_bwd, attn_bwd_workspace_size,
                    attn_decode_workspace_size, attn_device_error, attn_fwd, attn_fwd_chunked,
                    attn_kernel_launches, attn_status_string, kv_cache_append, load,
                    status_string)
 
 __all__ = [
-    "attn_fwd", "attn_fwd_chunked", "attn_decode", "attn_decode_workspace_size", "attn_decode_noalloc",
+    "attn_fwd", "attn_fwd_chunked", "attn_bwd", "attn_bwd_workspace_size", "attn_decode", "attn_decode_workspace_size", "attn_decode_noalloc",
     "kv_cache_append",
     "attn_status_string", "attn_kernel_launches", "attn_device_error", "AttnError",
     "load", "LIB_PATH",

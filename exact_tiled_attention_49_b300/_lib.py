@@ -25,6 +25,9 @@ SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _F, _P]),
     "attn_fwd_chunked": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
                               _P]),
+    "attn_bwd_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
+    "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P,
+                      _F, _P, ctypes.c_size_t, _P]),
     "attn_decode_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
                          ctypes.c_size_t, _P]),
@@ -184,6 +187,51 @@ def attn_fwd_chunked(q, kcache, vcache, q_pos, kv_lens, o=None, lse=None, causal
                               int(bool(causal)), float(scale), _stream(stream))
     _check(rc, "attn_fwd_chunked")
     return o, lse
+
+
+def attn_bwd_workspace_size(B: int, Hq: int, T: int) -> int:
+    return int(load().attn_bwd_workspace_size(B, Hq, T))
+
+
+def attn_bwd(q, k, v, o, dout, lse, causal=False, key_lens=None, q_pos=None, scale=None,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward pass: (dq, dk, dv) for attn_fwd's (o, lse) and the gradient
+    dout of its output.  q/o/dout [B,Hq,T,D], k/v [B,Hkv,S,D] (bf16, CUDA);
+    key_lens / q_pos as for attn_fwd / attn_fwd_chunked."""
+    lib = load()
+    B, Hq, T, D = q.shape
+    Bk, Hkv, S, Dk = k.shape
+    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q/k/v shape mismatch")
+    for t, name in ((o, "o"), (dout, "dout")):
+        if tuple(t.shape) != tuple(q.shape):
+            raise ValueError(f"{name} must have q's shape")
+    dt = _dtype_code(q)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    need = attn_bwd_workspace_size(B, Hq, T)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    ptrs = [_dev(q, "q", ndim=4), _dev(k, "k", ndim=4), _dev(v, "v", ndim=4),
+            _dev(o, "o", dtype=q.dtype, ndim=4), _dev(dout, "dout", dtype=q.dtype, ndim=4),
+            _dev(lse, "lse", dtype=torch.float32), _dev(dq, "dq", dtype=q.dtype, ndim=4),
+            _dev(dk, "dk", dtype=q.dtype, ndim=4), _dev(dv, "dv", dtype=q.dtype, ndim=4)]
+    if lse.numel() != B * Hq * T:
+        raise ValueError("lse must hold B*Hq*T floats")
+    kl = None
+    if key_lens is not None:
+        kl = _dev(key_lens, "key_lens", dtype=torch.int32, ndim=1)
+    qp = None
+    if q_pos is not None:
+        qp = _dev(q_pos, "q_pos", dtype=torch.int32, ndim=1)
+    rc = lib.attn_bwd(*ptrs, B, Hq, Hkv, T, S, D, dt, int(bool(causal)), kl, qp, float(scale),
+                      _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                      _stream(stream))
+    _check(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_decode_workspace_size(B: int, Hq: int, S_max: int, D: int) -> int:

@@ -17,6 +17,7 @@
 
 #include "../../include/attn.h"
 #include "append.cuh"
+#include "bwd_bf16_tc.cuh"
 #include "common.cuh"
 #include "decode.cuh"
 #include "fwd_bf16_tc.cuh"
@@ -206,6 +207,38 @@ int launch_fwd_f32(const void* q, const void* k, const void* v, void* o, float* 
   return launch_status();
 }
 
+// ------------------------------------------------------------- backward
+
+template <int D>
+int launch_bwd_tc(const attn::tcbwd::Params& p0, const void* q, const void* k, const void* v,
+                  const void* dout, cudaStream_t st) {
+  using namespace attn::tcbwd;
+  static std::atomic<uint64_t> smem_dq{0}, smem_dkdv{0};
+  auto kdq = bwd_dq_kernel<D>;
+  auto kdkdv = bwd_dkdv_kernel<D>;
+  if (!ensure_smem(kdq, Cfg<D>::kSmemAlloc, smem_dq) ||
+      !ensure_smem(kdkdv, Cfg<D>::kSmemAlloc, smem_dkdv))
+    return ATTN_ERR_CUDA;
+  CUtensorMap tq, tdo, tk, tv;
+  if (!make_tmap_bf16(&tq, q, D, p0.T, (long long)p0.B * p0.Hq) ||
+      !make_tmap_bf16(&tdo, dout, D, p0.T, (long long)p0.B * p0.Hq) ||
+      !make_tmap_bf16(&tk, k, D, p0.S, (long long)p0.B * p0.Hkv) ||
+      !make_tmap_bf16(&tv, v, D, p0.S, (long long)p0.B * p0.Hkv))
+    return ATTN_ERR_CUDA;
+  const long long rows = (long long)p0.B * p0.Hq * p0.T;
+  const long long want_blocks = (rows + 7) / 8;  // 8 warps per block, one row per warp
+  const unsigned blocks = (unsigned)std::min<long long>(want_blocks, (long long)num_sms() * 16);
+  bwd_delta_kernel<<<blocks, 256, 0, st>>>(p0, rows);
+  int rc = launch_status();
+  if (rc != ATTN_OK) return rc;
+  kdq<<<dim3(p0.n_qtiles, p0.Hq, p0.B), kThreads, Cfg<D>::kSmemAlloc, st>>>(tq, tdo, tk, tv, p0);
+  rc = launch_status();
+  if (rc != ATTN_OK) return rc;
+  kdkdv<<<dim3(p0.n_ktiles, p0.Hkv, p0.B), kThreads, Cfg<D>::kSmemAlloc, st>>>(tq, tdo, tk, tv,
+                                                                              p0);
+  return launch_status();
+}
+
 // -------------------------------------------------------------- decode
 
 template <typename T, int D, int G>
@@ -314,6 +347,52 @@ int attn_fwd_chunked(const void* q, const void* kcache, const void* vcache, void
   if (!q_pos || !kv_lens) return ATTN_ERR_INVALID_ARG;
   return fwd_dispatch(q, kcache, vcache, o, lse, B, Hq, Hkv, T, S_max, D, dtype, causal, kv_lens,
                       q_pos, scale, stream);
+}
+
+size_t attn_bwd_workspace_size(int B, int Hq, int T) {
+  if (B <= 0 || Hq <= 0 || T <= 0) return 0;
+  return ((size_t)B * Hq * T * sizeof(float) + 15) / 16 * 16;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+             const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int T, int S,
+             int D, int dtype, int causal, const int32_t* key_lens, const int32_t* q_pos,
+             float scale, void* workspace, size_t ws_bytes, attn_stream_t stream) {
+  if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || S <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !finite_positive(scale)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (B > 65535 || Hq > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned4(lse) ||
+      (key_lens != nullptr && !aligned4(key_lens)) || (q_pos != nullptr && !aligned4(q_pos)))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t need = attn_bwd_workspace_size(B, Hq, T);
+  if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+  attn::tcbwd::Params p{};
+  p.o = o;
+  p.dout = dout;
+  p.lse = lse;
+  p.delta = static_cast<float*>(workspace);
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.key_lens = key_lens;
+  p.q_pos = q_pos;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.T = T;
+  p.S = S;
+  p.D = D;
+  p.causal = causal ? 1 : 0;
+  p.n_qtiles = (T + attn::tcbwd::kBM - 1) / attn::tcbwd::kBM;
+  p.n_ktiles = (S + attn::tcbwd::kBM - 1) / attn::tcbwd::kBM;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return D == 64 ? launch_bwd_tc<64>(p, q, k, v, dout, st) : launch_bwd_tc<128>(p, q, k, v, dout, st);
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int S_max, int D) {

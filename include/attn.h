@@ -133,6 +133,53 @@ ATTN_API int attn_fwd_chunked(const void* q, const void* kcache, const void* vca
                               int causal, float scale, attn_stream_t stream);
 
 /*
+ * attn_bwd_workspace_size -- bytes of device scratch attn_bwd needs (one
+ * float per query row: delta = rowsum(dO * O)).  Returns 0 for invalid
+ * sizes.
+ */
+ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int T);
+
+/*
+ * attn_bwd -- backward pass: dQ, dK, dV of the attention computed by attn_fwd
+ * (or attn_fwd_chunked with the same q_pos), given dO and the forward's O
+ * and LSE.  "Hands-on build guide: FlashAttention-style tiled attention
+ * kernel in pure NumPy", Roadmap (gradient through attention by the chain
+ * rule through the softmax); "Self-Attention: Implementation, Complexity,
+ * and Efficient Variants", FlashAttention (the backward recomputes the
+ * attention weights on chip instead of storing them):
+ *
+ *   P = exp(scale * Q K^T - LSE) on visible entries (0 elsewhere)
+ *   dV = P^T dO,  dP = dO V^T,  delta = rowsum(dO * O)
+ *   dS = P (dP - delta),  dQ = scale dS K,  dK = scale dS^T Q
+ *
+ * with the query heads of a GQA group summed into their KV head.  Padded
+ * rows and rows that see no key take no part (their output is the constant
+ * 0): their dQ is 0 and they add nothing to dK, dV.  Keys no row sees get
+ * dK = dV = 0.  K/V rows at or past the valid length are never used.
+ *
+ *   q, o, dout  [B,Hq,T,D]   dtype (read)        dout must be finite
+ *   k, v        [B,Hkv,S,D]  dtype (read)
+ *   lse         [B,Hq,T]     float32 (read: attn_fwd's LSE for these inputs)
+ *   dq          [B,Hq,T,D]   dtype (written)
+ *   dk, dv      [B,Hkv,S,D]  dtype (written)
+ *   key_lens, q_pos, causal, scale: as for attn_fwd / attn_fwd_chunked
+ *                            (q_pos NULL = bottom-right, S - T)
+ *   workspace   >= attn_bwd_workspace_size(B, Hq, T) bytes, 16-byte aligned
+ *
+ * Supported: ATTN_BF16 with D in {64, 128} (tcgen05 tensor cores, fp32
+ * accumulation; P and dS are rounded to bf16 for the products); all
+ * pointers 16-byte aligned (lse, key_lens, q_pos: 4).  ATTN_F32 returns
+ * ATTN_ERR_UNSUPPORTED.  No atomics: results do not depend on scheduling.
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
+ * ATTN_ERR_WORKSPACE or ATTN_ERR_CUDA.
+ */
+ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o,
+                      const void* dout, const float* lse, void* dq, void* dk, void* dv, int B,
+                      int Hq, int Hkv, int T, int S, int D, int dtype, int causal,
+                      const int32_t* key_lens, const int32_t* q_pos, float scale,
+                      void* workspace, size_t ws_bytes, attn_stream_t stream);
+
+/*
  * attn_decode_workspace_size -- bytes of device scratch attn_decode needs for
  * a batch of B sequences, Hq query heads, caches of S_max positions and head
  * size D.  The caller allocates it (any alignment >= 16 bytes) and may reuse

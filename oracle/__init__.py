@@ -20,11 +20,12 @@ import os
 
 import numpy as np
 
-from .oracle_np import (attn_bwd_np, attn_decode_np, attn_fwd_np, attn_tiled_online_np,
+from .oracle_np import (attn_bwd_magnitudes_np, attn_bwd_np, attn_decode_np, attn_fwd_np, attn_tiled_online_np,
                         bf16_bits_to_f64, visibility)
 
 __all__ = [
     "attn_fwd", "attn_decode", "kv_append", "attn_fwd_np", "attn_decode_np", "attn_bwd_np",
+    "attn_bwd_magnitudes_np",
     "attn_tiled_online_np", "bf16_bits_to_f64", "visibility", "build",
     "default_threads",
 ]

@@ -236,3 +236,54 @@ def attn_bwd_np(q, k, v, do, causal=False, key_lens=None, scale=None, bf16=False
             dq[b, h] = scale * (ds @ kg)
             dk[b, g] += scale * (ds.T @ q[b, h])
     return dq, dk, dv, o, lse
+
+
+def attn_bwd_magnitudes_np(q, k, v, do, causal=False, key_lens=None, scale=None, bf16=False,
+                           q_pos=None):
+    """Per-element magnitudes that bound the rounding error of a bf16
+    evaluation of the backward (test infrastructure for tolerances).
+
+    With u = 2^-9 (one bf16 rounding), a kernel that rounds P and dS to bf16
+    before the products, forms delta from the bf16-rounded O and rounds
+    each result once has, to first order, an error of at most u times:
+
+        A_dq = scale * (|dS| |K| + (P |K|) * rowsum(|dO * O|)) + |dQ|
+        A_dk = scale * (|dS|^T |Q| + P^T (|Q| * rowsum(|dO * O|))) + |dK|
+        A_dv = P^T |dO| + |dV|
+
+    (the first terms: rounding of dS; the second: the error of delta,
+    rowsum(dO * O) with O rounded; the last: rounding of the result).
+    Returns (A_dq, A_dk, A_dv) in the shapes of dq, dk, dv.
+    """
+    q, k, v, do = (_as_f64(x, bf16) for x in (q, k, v, do))
+    B, Hq, T, D = q.shape
+    _, Hkv, S, _ = k.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    G = Hq // Hkv
+    aq = np.zeros_like(q)
+    ak = np.zeros_like(k)
+    av = np.zeros_like(v)
+    dq, dk, dv, o, _ = attn_bwd_np(q, k, v, do, causal=causal, key_lens=key_lens, scale=scale,
+                                   q_pos=q_pos)
+    for b in range(B):
+        L = S if key_lens is None else int(key_lens[b])
+        _, vis = visibility(T, S, L, causal, None if q_pos is None else int(q_pos[b]))
+        has = vis.any(axis=1)
+        keys = vis.any(axis=0)
+        for h in range(Hq):
+            g = h // G
+            kg = np.where(keys[:, None], k[b, g], 0.0)
+            vg = np.where(keys[:, None], v[b, g], 0.0)
+            s = np.where(vis, (q[b, h] @ kg.T) * scale, _NEG_INF)
+            m = np.where(has, s.max(axis=1), 0.0)
+            e = np.where(vis, np.exp(s - m[:, None]), 0.0)
+            p = e / np.where(has, e.sum(axis=1), 1.0)[:, None]
+            dp = do[b, h] @ vg.T
+            delta = (do[b, h] * o[b, h]).sum(axis=1)
+            ads = np.abs(p * (dp - delta[:, None]))
+            rdo = np.abs(do[b, h] * o[b, h]).sum(axis=1)          # rowsum |dO * O|
+            aq[b, h] = scale * (ads @ np.abs(kg) + (p @ np.abs(kg)) * rdo[:, None])
+            ak[b, g] += scale * (ads.T @ np.abs(q[b, h]) + p.T @ (np.abs(q[b, h]) * rdo[:, None]))
+            av[b, g] += p.T @ np.abs(do[b, h])
+    return aq + np.abs(dq), ak + np.abs(dk), av + np.abs(dv)
