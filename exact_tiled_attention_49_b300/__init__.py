@@ -8,7 +8,7 @@ with GQA/MQA head sharing, and an O(1) KV-cache append.
 The work is done by hand-written CUDA kernels in ``libattn.so`` behind a C
 ABI (``include/attn.h``); this package is a thin ctypes binding of it.
 """
-from ._lib import (ATTN_BF16, ATTN_ERR_CUDA, ATTN_ERR_INVALID_ARG,  # noqa: F401
+from ._lib import (ATTN_BF16, ATTN_ERR_CUDA, ATTN_F16, ATTN_ERR_INVALID_ARG,  # noqa: F401
                    ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_F32, ATTN_OK,
                    LIB_PATH, NOALLOC_SCRATCH_BYTES, SIGNATURES, AttnError, attn_decode,
                    attn_decode_noalloc,

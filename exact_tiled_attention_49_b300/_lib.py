@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libattn.so")
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_ERR_CUDA = range(5)
-ATTN_F32, ATTN_BF16 = 0, 1
+ATTN_F32, ATTN_BF16, ATTN_F16 = 0, 1, 2
 
 # Every entry point declared in include/attn.h, with its ctypes signature.
 _P, _I, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
@@ -81,9 +81,11 @@ def _check(rc: int, what: str):
 def _dtype_code(t: torch.Tensor) -> int:
     if t.dtype == torch.bfloat16:
         return ATTN_BF16
+    if t.dtype == torch.float16:
+        return ATTN_F16
     if t.dtype == torch.float32:
         return ATTN_F32
-    raise TypeError(f"unsupported dtype {t.dtype}; expected bfloat16 or float32")
+    raise TypeError(f"unsupported dtype {t.dtype}; expected bfloat16, float16 or float32")
 
 
 def _dev(t: torch.Tensor, name: str, dtype=None, ndim=None):

@@ -53,31 +53,36 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 3-D bf16 tensor [outer, rows, D] (D contiguous) loaded as boxes of
-// 64 columns x 128 rows with 128-byte swizzle; rows past `rows` read as 0.
-bool make_tmap_bf16(CUtensorMap* m, const void* base, int D, int rows, long long outer) {
+// 3-D 16-bit tensor [outer, rows, D] (D contiguous; bf16, or fp16 when f16)
+// loaded as boxes of 64 columns x 128 rows with 128-byte swizzle; rows past
+// `rows` read as 0.
+bool make_tmap_bf16(CUtensorMap* m, const void* base, int D, int rows, long long outer,
+                    bool f16 = false) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)outer};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)rows * (cuuint64_t)D * 2};
   cuuint32_t box[3] = {64, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-// 2-D bf16 tensor [rows, D] (D contiguous) loaded as boxes of 64 columns x
-// `box_rows` rows with 128-byte swizzle.
-bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, int D, long long rows, int box_rows) {
+// 2-D 16-bit tensor [rows, D] (D contiguous; bf16, or fp16 when f16) loaded
+// as boxes of 64 columns x `box_rows` rows with 128-byte swizzle.
+bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, int D, long long rows, int box_rows,
+                       bool f16 = false) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)D * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  CUresult r = fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -141,18 +146,18 @@ int launch_status() {
 
 // ------------------------------------------------------------- prefill
 
-template <int D>
+template <int D, bool kF16>
 int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                   int Hq, int Hkv, int T, int S, int causal, const int32_t* key_lens,
                   const int32_t* q_pos, float scale, cudaStream_t st) {
   using namespace attn::tcfwd;
   static std::atomic<uint64_t> smem_done{0};
-  auto kernel = fwd_bf16_tc_kernel<D>;
+  auto kernel = fwd_bf16_tc_kernel<D, kF16>;
   if (!ensure_smem(kernel, Cfg<D>::kSmemAlloc, smem_done)) return ATTN_ERR_CUDA;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_bf16(&tq, q, D, T, (long long)B * Hq) ||
-      !make_tmap_bf16(&tk, k, D, S, (long long)B * Hkv) ||
-      !make_tmap_bf16(&tv, v, D, S, (long long)B * Hkv))
+  if (!make_tmap_bf16(&tq, q, D, T, (long long)B * Hq, kF16) ||
+      !make_tmap_bf16(&tk, k, D, S, (long long)B * Hkv, kF16) ||
+      !make_tmap_bf16(&tv, v, D, S, (long long)B * Hkv, kF16))
     return ATTN_ERR_CUDA;
   Params p;
   p.o = o;
@@ -209,26 +214,26 @@ int launch_fwd_f32(const void* q, const void* k, const void* v, void* o, float* 
 
 // ------------------------------------------------------------- backward
 
-template <int D>
+template <int D, bool kF16>
 int launch_bwd_tc(const attn::tcbwd::Params& p0, const void* q, const void* k, const void* v,
                   const void* dout, cudaStream_t st) {
   using namespace attn::tcbwd;
   static std::atomic<uint64_t> smem_dq{0}, smem_dkdv{0};
-  auto kdq = bwd_dq_kernel<D>;
-  auto kdkdv = bwd_dkdv_kernel<D>;
+  auto kdq = bwd_dq_kernel<D, kF16>;
+  auto kdkdv = bwd_dkdv_kernel<D, kF16>;
   if (!ensure_smem(kdq, Cfg<D>::kSmemAlloc, smem_dq) ||
       !ensure_smem(kdkdv, Cfg<D>::kSmemAlloc, smem_dkdv))
     return ATTN_ERR_CUDA;
   CUtensorMap tq, tdo, tk, tv;
-  if (!make_tmap_bf16(&tq, q, D, p0.T, (long long)p0.B * p0.Hq) ||
-      !make_tmap_bf16(&tdo, dout, D, p0.T, (long long)p0.B * p0.Hq) ||
-      !make_tmap_bf16(&tk, k, D, p0.S, (long long)p0.B * p0.Hkv) ||
-      !make_tmap_bf16(&tv, v, D, p0.S, (long long)p0.B * p0.Hkv))
+  if (!make_tmap_bf16(&tq, q, D, p0.T, (long long)p0.B * p0.Hq, kF16) ||
+      !make_tmap_bf16(&tdo, dout, D, p0.T, (long long)p0.B * p0.Hq, kF16) ||
+      !make_tmap_bf16(&tk, k, D, p0.S, (long long)p0.B * p0.Hkv, kF16) ||
+      !make_tmap_bf16(&tv, v, D, p0.S, (long long)p0.B * p0.Hkv, kF16))
     return ATTN_ERR_CUDA;
   const long long rows = (long long)p0.B * p0.Hq * p0.T;
   const long long want_blocks = (rows + 7) / 8;  // 8 warps per block, one row per warp
   const unsigned blocks = (unsigned)std::min<long long>(want_blocks, (long long)num_sms() * 16);
-  bwd_delta_kernel<<<blocks, 256, 0, st>>>(p0, rows);
+  bwd_delta_kernel<kF16><<<blocks, 256, 0, st>>>(p0, rows);
   int rc = launch_status();
   if (rc != ATTN_OK) return rc;
   kdq<<<dim3(p0.n_qtiles, p0.Hq, p0.B), kThreads, Cfg<D>::kSmemAlloc, st>>>(tq, tdo, tk, tv, p0);
@@ -244,17 +249,18 @@ int launch_bwd_tc(const attn::tcbwd::Params& p0, const void* q, const void* k, c
 template <typename T, int D, int G>
 int launch_decode_g(const attn::decode::Params& p, cudaStream_t st) {
   using namespace attn::decode;
-  if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-    // bf16: persistent tensor-core workers, one CTA per SM at most
+  if constexpr (!std::is_same<T, float>::value) {
+    // bf16 / fp16: persistent tensor-core workers, one CTA per SM at most
+    constexpr bool kF16 = std::is_same<T, __half>::value;
     using C = MmaCfg<D, G>;
     static std::atomic<uint64_t> smem_done{0};
-    auto kernel = decode_split_mma_kernel<D, G>;
+    auto kernel = decode_split_mma_kernel<D, G, kF16>;
     if (!ensure_smem(kernel, C::kSmemBytes, smem_done)) return ATTN_ERR_CUDA;
     const long long rows = (long long)p.B * p.Hkv * p.S_max;
     if (rows >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
     CUtensorMap tk, tv;
-    if (!make_tmap_bf16_2d(&tk, p.kc, D, rows, C::kSub) ||
-        !make_tmap_bf16_2d(&tv, p.vc, D, rows, C::kSub))
+    if (!make_tmap_bf16_2d(&tk, p.kc, D, rows, C::kSub, kF16) ||
+        !make_tmap_bf16_2d(&tv, p.vc, D, rows, C::kSub, kF16))
       return ATTN_ERR_CUDA;
     const long long items = (long long)p.splits * p.B * p.Hkv;
     long long ctas = std::min<long long>(num_sms(), (items + C::kWarps - 1) / C::kWarps);
@@ -301,15 +307,19 @@ int fwd_dispatch(const void* q, const void* k, const void* v, void* o, float* ls
   if (key_lens != nullptr && !aligned4(key_lens)) return ATTN_ERR_INVALID_ARG;
   if (q_pos != nullptr && !aligned4(q_pos)) return ATTN_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (dtype == ATTN_BF16) {
+  if (dtype == ATTN_BF16 || dtype == ATTN_F16) {
     if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
       return ATTN_ERR_INVALID_ARG;
-    if (D == 64)
-      return launch_fwd_tc<64>(q, k, v, o, lse, B, Hq, Hkv, T, S, causal, key_lens, q_pos, scale,
-                               st);
-    return launch_fwd_tc<128>(q, k, v, o, lse, B, Hq, Hkv, T, S, causal, key_lens, q_pos, scale,
-                              st);
+    const bool f16 = dtype == ATTN_F16;
+#define ATTN_TC_CASE(DD, F)                                                                  \
+  return launch_fwd_tc<DD, F>(q, k, v, o, lse, B, Hq, Hkv, T, S, causal, key_lens, q_pos, \
+                              scale, st);
+    if (D == 64) {
+      if (f16) ATTN_TC_CASE(64, true) else ATTN_TC_CASE(64, false)
+    }
+    if (f16) ATTN_TC_CASE(128, true) else ATTN_TC_CASE(128, false)
+#undef ATTN_TC_CASE
   }
   if (dtype == ATTN_F32) {
     if (D > 256) return ATTN_ERR_UNSUPPORTED;
@@ -361,8 +371,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || S <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0 || !finite_positive(scale)) return ATTN_ERR_INVALID_ARG;
-  if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
-  if (dtype != ATTN_BF16 || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
+  if (dtype != ATTN_BF16 && dtype != ATTN_F16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  if (dtype == ATTN_F32 || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
   if (B > 65535 || Hq > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned4(lse) ||
@@ -392,7 +402,11 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  return D == 64 ? launch_bwd_tc<64>(p, q, k, v, dout, st) : launch_bwd_tc<128>(p, q, k, v, dout, st);
+  if (dtype == ATTN_F16)
+    return D == 64 ? launch_bwd_tc<64, true>(p, q, k, v, dout, st)
+                   : launch_bwd_tc<128, true>(p, q, k, v, dout, st);
+  return D == 64 ? launch_bwd_tc<64, false>(p, q, k, v, dout, st)
+                 : launch_bwd_tc<128, false>(p, q, k, v, dout, st);
 }
 
 size_t attn_decode_workspace_size(int B, int Hq, int S_max, int D) {
@@ -406,7 +420,7 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, const int
   if (!q || !kcache || !vcache || !kv_lens || !o) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || S_max <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0 || !finite_positive(scale)) return ATTN_ERR_INVALID_ARG;
-  if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_F16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   const int G = Hq / Hkv;
   if (G > 16 || (G & (G - 1)) != 0) return ATTN_ERR_UNSUPPORTED;
@@ -438,6 +452,9 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, const int
   if (dtype == ATTN_BF16) {
     return D == 64 ? launch_decode_d<__nv_bfloat16, 64>(p, G, st)
                    : launch_decode_d<__nv_bfloat16, 128>(p, G, st);
+  }
+  if (dtype == ATTN_F16) {
+    return D == 64 ? launch_decode_d<__half, 64>(p, G, st) : launch_decode_d<__half, 128>(p, G, st);
   }
   return D == 64 ? launch_decode_d<float, 64>(p, G, st) : launch_decode_d<float, 128>(p, G, st);
 }
@@ -494,7 +511,7 @@ int kv_cache_append(void* kcache, void* vcache, const void* k_new, const void* v
   if (!kcache || !vcache || !k_new || !v_new || !pos) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || Hkv <= 0 || S_max <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   size_t esz;
-  if (dtype == ATTN_BF16) esz = 2;
+  if (dtype == ATTN_BF16 || dtype == ATTN_F16) esz = 2;
   else if (dtype == ATTN_F32) esz = 4;
   else return ATTN_ERR_INVALID_ARG;
   const size_t row_bytes = (size_t)D * esz;

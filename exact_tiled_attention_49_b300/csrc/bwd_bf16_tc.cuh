@@ -1,4 +1,5 @@
-// bwd_bf16_tc.cuh -- attention backward (dQ, dK, dV) on the tensor cores.
+// bwd_bf16_tc.cuh -- attention backward (dQ, dK, dV) on the tensor cores, bf16
+// or fp16 (kF16) inputs and gradients.
 //
 // The chain rule through the softmax ("Hands-on build guide:
 // FlashAttention-style tiled attention kernel in pure NumPy", Roadmap:
@@ -67,25 +68,26 @@ __device__ __forceinline__ int q_offset(const Params& p, int b) {
 
 // ------------------------------------------------------------ delta pass
 // One warp per row: delta[row] = sum_d dO[row,d] * O[row,d] in fp32.
+template <bool kF16>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(Params p, long long rows) {
   const long long warp_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const long long n_warps = ((long long)gridDim.x * blockDim.x) >> 5;
   for (long long r = warp_id; r < rows; r += n_warps) {
-    const __nv_bfloat16* orow = reinterpret_cast<const __nv_bfloat16*>(p.o) + r * p.D;
-    const __nv_bfloat16* drow = reinterpret_cast<const __nv_bfloat16*>(p.dout) + r * p.D;
+    const uint16_t* orow = reinterpret_cast<const uint16_t*>(p.o) + r * p.D;
+    const uint16_t* drow = reinterpret_cast<const uint16_t*>(p.dout) + r * p.D;
     float acc = 0.f;
     for (int d = lane * 8; d < p.D; d += 256) {
       const uint4 a = *reinterpret_cast<const uint4*>(orow + d);
       const uint4 g = *reinterpret_cast<const uint4*>(drow + d);
-      acc = fmaf(bf16_lo(a.x), bf16_lo(g.x), acc);
-      acc = fmaf(bf16_hi(a.x), bf16_hi(g.x), acc);
-      acc = fmaf(bf16_lo(a.y), bf16_lo(g.y), acc);
-      acc = fmaf(bf16_hi(a.y), bf16_hi(g.y), acc);
-      acc = fmaf(bf16_lo(a.z), bf16_lo(g.z), acc);
-      acc = fmaf(bf16_hi(a.z), bf16_hi(g.z), acc);
-      acc = fmaf(bf16_lo(a.w), bf16_lo(g.w), acc);
-      acc = fmaf(bf16_hi(a.w), bf16_hi(g.w), acc);
+      acc = fmaf(elem_lo<kF16>(a.x), elem_lo<kF16>(g.x), acc);
+      acc = fmaf(elem_hi<kF16>(a.x), elem_hi<kF16>(g.x), acc);
+      acc = fmaf(elem_lo<kF16>(a.y), elem_lo<kF16>(g.y), acc);
+      acc = fmaf(elem_hi<kF16>(a.y), elem_hi<kF16>(g.y), acc);
+      acc = fmaf(elem_lo<kF16>(a.z), elem_lo<kF16>(g.z), acc);
+      acc = fmaf(elem_hi<kF16>(a.z), elem_hi<kF16>(g.z), acc);
+      acc = fmaf(elem_lo<kF16>(a.w), elem_lo<kF16>(g.w), acc);
+      acc = fmaf(elem_hi<kF16>(a.w), elem_hi<kF16>(g.w), acc);
     }
     acc = warp_sum(acc);
     if (lane == 0) p.delta[r] = acc;
@@ -119,7 +121,7 @@ struct Cfg {
 //
 // TMEM: S at column 0 (dS packed over its first 64 columns), dP at 128,
 // dQ at 256.
-template <int D>
+template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_do,
@@ -241,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc_ss = idesc_bf16(kBM, kBM, false, false);   // M=N=128, K-major
-    constexpr uint32_t idesc_ts = idesc_bf16(kBM, D, false, true);      // B MN-major, N = D
+    constexpr uint32_t idesc_ss = idesc_f16kind(kBM, kBM, false, false, kF16);   // M=N=128, K-major
+    constexpr uint32_t idesc_ts = idesc_f16kind(kBM, D, false, true, kF16);      // B MN-major, N = D
     const uint64_t dq_a = sdesc_sw128(s_q, 16, 1024), ddo_a = sdesc_sw128(s_do, 16, 1024);
     const uint64_t dk0 = sdesc_sw128(s_ring, 16, 1024);
     const uint64_t dkmn0 = sdesc_sw128(s_ring, C::kChunkBytes, 1024);
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p1 = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), sl2, -lse2));
           const float d0 = (kj < lim) ? p0 * (__uint_as_float(dp[e]) - dlt) : 0.f;
           const float d1 = (kj + 1 < lim) ? p1 * (__uint_as_float(dp[e + 1]) - dlt) : 0.f;
-          pk[e >> 1] = pack_bf16x2(d0, d1);
+          pk[e >> 1] = pack2<kF16>(d0, d1);
         }
         tmem_st16(lane_base + kColS + 16 * c, pk);
       }
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool has = ok && n > 0;  // warp-uniform
     if (has) tc_fence_after();
     const float sc = row_ok ? p.scale : 0.f;
-    __nv_bfloat16* drow = reinterpret_cast<__nv_bfloat16*>(p.dq) + row * D;
+    uint16_t* drow = reinterpret_cast<uint16_t*>(p.dq) + row * D;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {
       uint32_t a[32];
@@ -359,10 +361,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int v4 = 0; v4 < 4; ++v4) {
           uint4 u = make_uint4(0, 0, 0, 0);
           if (has) {
-            u.x = pack_bf16x2(__uint_as_float(a[8 * v4 + 0]) * sc, __uint_as_float(a[8 * v4 + 1]) * sc);
-            u.y = pack_bf16x2(__uint_as_float(a[8 * v4 + 2]) * sc, __uint_as_float(a[8 * v4 + 3]) * sc);
-            u.z = pack_bf16x2(__uint_as_float(a[8 * v4 + 4]) * sc, __uint_as_float(a[8 * v4 + 5]) * sc);
-            u.w = pack_bf16x2(__uint_as_float(a[8 * v4 + 6]) * sc, __uint_as_float(a[8 * v4 + 7]) * sc);
+            u.x = pack2<kF16>(__uint_as_float(a[8 * v4 + 0]) * sc, __uint_as_float(a[8 * v4 + 1]) * sc);
+            u.y = pack2<kF16>(__uint_as_float(a[8 * v4 + 2]) * sc, __uint_as_float(a[8 * v4 + 3]) * sc);
+            u.z = pack2<kF16>(__uint_as_float(a[8 * v4 + 4]) * sc, __uint_as_float(a[8 * v4 + 5]) * sc);
+            u.w = pack2<kF16>(__uint_as_float(a[8 * v4 + 6]) * sc, __uint_as_float(a[8 * v4 + 7]) * sc);
           }
           reinterpret_cast<uint4*>(drow + 32 * c)[v4] = u;
         }
@@ -382,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 //
 // TMEM: S^T at column 0 (P^T packed over its first 64 columns), dP^T at 128
 // (dS^T packed over its first 64), dV at 256, dK at 256 + D.
-template <int D>
+template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_do,
@@ -481,8 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc_ss = idesc_bf16(kBM, kBM, false, false);
-    constexpr uint32_t idesc_ts = idesc_bf16(kBM, D, false, true);
+    constexpr uint32_t idesc_ss = idesc_f16kind(kBM, kBM, false, false, kF16);
+    constexpr uint32_t idesc_ts = idesc_f16kind(kBM, D, false, true, kF16);
     const uint64_t dk_a = sdesc_sw128(s_k, 16, 1024), dv_a = sdesc_sw128(s_v, 16, 1024);
     const uint64_t dr0 = sdesc_sw128(s_ring, 16, 1024);
     const uint64_t drmn0 = sdesc_sw128(s_ring, C::kChunkBytes, 1024);
@@ -590,8 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p0 = v0 ? e0 : 0.f, p1 = v1 ? e1 : 0.f;
           const float d0 = v0 ? e0 * (__uint_as_float(dp[e]) - st_dlt[col]) : 0.f;
           const float d1 = v1 ? e1 * (__uint_as_float(dp[e + 1]) - st_dlt[col + 1]) : 0.f;
-          ppk[e >> 1] = pack_bf16x2(p0, p1);
-          dpk[e >> 1] = pack_bf16x2(d0, d1);
+          ppk[e >> 1] = pack2<kF16>(p0, p1);
+          dpk[e >> 1] = pack2<kF16>(d0, d1);
         }
         tmem_st16(lane_base + kColS + 16 * c, ppk);
         tmem_st16(lane_base + kColDP + 16 * c, dpk);
@@ -607,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t krow = ((size_t)b * p.Hkv + g) * p.S + kj;
 #pragma unroll
     for (int which = 0; which < 2; ++which) {  // 0: dV, 1: dK
-      __nv_bfloat16* drow = reinterpret_cast<__nv_bfloat16*>(which ? p.dk : p.dv) + krow * D;
+      uint16_t* drow = reinterpret_cast<uint16_t*>(which ? p.dk : p.dv) + krow * D;
       const float sc = which ? p.scale : 1.f;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -621,10 +623,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int v4 = 0; v4 < 4; ++v4) {
             uint4 w = make_uint4(0, 0, 0, 0);
             if (has) {
-              w.x = pack_bf16x2(__uint_as_float(a[8 * v4 + 0]) * sc, __uint_as_float(a[8 * v4 + 1]) * sc);
-              w.y = pack_bf16x2(__uint_as_float(a[8 * v4 + 2]) * sc, __uint_as_float(a[8 * v4 + 3]) * sc);
-              w.z = pack_bf16x2(__uint_as_float(a[8 * v4 + 4]) * sc, __uint_as_float(a[8 * v4 + 5]) * sc);
-              w.w = pack_bf16x2(__uint_as_float(a[8 * v4 + 6]) * sc, __uint_as_float(a[8 * v4 + 7]) * sc);
+              w.x = pack2<kF16>(__uint_as_float(a[8 * v4 + 0]) * sc, __uint_as_float(a[8 * v4 + 1]) * sc);
+              w.y = pack2<kF16>(__uint_as_float(a[8 * v4 + 2]) * sc, __uint_as_float(a[8 * v4 + 3]) * sc);
+              w.z = pack2<kF16>(__uint_as_float(a[8 * v4 + 4]) * sc, __uint_as_float(a[8 * v4 + 5]) * sc);
+              w.w = pack2<kF16>(__uint_as_float(a[8 * v4 + 6]) * sc, __uint_as_float(a[8 * v4 + 7]) * sc);
             }
             reinterpret_cast<uint4*>(drow + 32 * c)[v4] = w;
           }

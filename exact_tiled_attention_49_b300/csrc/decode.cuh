@@ -94,6 +94,7 @@ __device__ __forceinline__ void load_lane<float, 2>(const float* row, int lane, 
 
 __device__ __forceinline__ void store_out(float* o, float x) { *o = x; }
 __device__ __forceinline__ void store_out(__nv_bfloat16* o, float x) { *o = __float2bfloat16_rn(x); }
+__device__ __forceinline__ void store_out(__half* o, float x) { *o = __float2half_rn(x); }
 
 template <typename T, int D, int G>
 __host__ __device__ constexpr size_t split_smem_bytes() {
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Params p) {
 }
 
 // ---------------------------------------------------------------------------
-// bf16 pass 1: persistent streaming workers on the tensor cores.
+// bf16 / fp16 pass 1: persistent streaming workers on the tensor cores.
 //
 // Item virtual index is chunk-major, i = chunk * (B * Hkv) + b * Hkv + g;
 // items whose chunk starts at or past kv_lens[b] are skipped.  Every warp of
@@ -229,8 +230,9 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Params p) {
 // online softmax runs on the accumulator fragments (each thread holds 8
 // scores of rows g and g + 8, the 4 threads of a row group finish the
 // reductions with two shuffles); O += P V reuses the score fragments as the
-// bf16 A operand, with V fragments from ldmatrix.trans.  Scores are scaled
-// in fp32 (scale * log2 e) so that q keeps its exact bf16 values.
+// A operand (rounded to the input type), with V fragments from
+// ldmatrix.trans.  Scores are scaled in fp32 (scale * log2 e) so that q keeps
+// its exact input values.
 struct Cursor {
   int item;  // virtual item index, or -1 when the worker's stream is exhausted
   int j;     // 32-key sub-tile within the item
@@ -298,20 +300,31 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
-// d (16x8 fp32) += a (16x16 bf16, row) * b (16x8 bf16, col)
-__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+// d (16x8 fp32) += a (16x16, row) * b (16x8, col); a and b both bf16, or
+// both fp16 when kF16.
+template <bool kF16>
+__device__ __forceinline__ void mma16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  if constexpr (kF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+  }
 }
 // Byte offset of 16-byte slot c (0..7) of row r in a 128B-swizzled tile.
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-template <int D, int G>
+// kF16: fp16 cache and query (else bf16).
+template <int D, int G, bool kF16>
 __global__ void __launch_bounds__(32 * MmaCfg<D, G>::kWarps)
     decode_split_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, Params p) {
@@ -362,7 +375,7 @@ __global__ void __launch_bounds__(32 * MmaCfg<D, G>::kWarps)
         const int qb = items_issued & 1;
         mbar_arrive_expect_tx(bar_q + 8 * qb, C::kQRawBytes);
         bulk_load(qraw + qb * C::kQRawStride,
-                  reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                  reinterpret_cast<const uint16_t*>(p.q) +
                       ((size_t)c.b * p.Hq + (size_t)c.g * G) * D,
                   C::kQRawBytes, bar_q + 8 * qb);
       }
@@ -443,8 +456,8 @@ __global__ void __launch_bounds__(32 * MmaCfg<D, G>::kWarps)
         const int m = lane >> 3, r = nt * 8 + (lane & 7), cg = 4 * u + m;
         uint32_t b0, b1, b2, b3;
         ldsm_x4(kst + (cg >> 3) * C::kTileBytes + sw128(r, cg & 7), b0, b1, b2, b3);
-        mma_bf16(sacc[nt], qa[2 * u], b0, b1);
-        mma_bf16(sacc[nt], qa[2 * u + 1], b2, b3);
+        mma16<kF16>(sacc[nt], qa[2 * u], b0, b1);
+        mma16<kF16>(sacc[nt], qa[2 * u + 1], b2, b3);
       }
     }
     // Online softmax on the fragments: element e of n-tile nt is row
@@ -488,8 +501,8 @@ __global__ void __launch_bounds__(32 * MmaCfg<D, G>::kWarps)
       const float p3 = ex2_approx(sacc[nt][3] - m_run[1]);
       l_run[0] += p0 + p1;
       l_run[1] += p2 + p3;
-      pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p0, p1);
-      pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2, p3);
+      pa[nt >> 1][(nt & 1) * 2 + 0] = pack2<kF16>(p0, p1);
+      pa[nt >> 1][(nt & 1) * 2 + 1] = pack2<kF16>(p2, p3);
     }
     // O += P V: 2 k-steps of 16 keys, NT n-tiles of 8 output columns.
 #pragma unroll
@@ -500,8 +513,8 @@ __global__ void __launch_bounds__(32 * MmaCfg<D, G>::kWarps)
         const int r = ks * 16 + (m & 1) * 8 + (lane & 7), cg = 2 * v + (m >> 1);
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(vst + (cg >> 3) * C::kTileBytes + sw128(r, cg & 7), b0, b1, b2, b3);
-        mma_bf16(o[2 * v], pa[ks], b0, b1);
-        mma_bf16(o[2 * v + 1], pa[ks], b2, b3);
+        mma16<kF16>(o[2 * v], pa[ks], b0, b1);
+        mma16<kF16>(o[2 * v + 1], pa[ks], b2, b3);
       }
     }
     __syncwarp();  // the stage may be refilled from here on

@@ -1,4 +1,5 @@
-// fwd_bf16_tc.cuh -- bf16 prefill forward on the 5th-generation tensor cores.
+// fwd_bf16_tc.cuh -- bf16 / fp16 prefill forward on the 5th-generation tensor
+// cores.
 //
 // The method ("FlashAttention", Transformers in Action section 9.4.1 and
 // Figure 9.8; "Implementing attention from scratch", Core ideas, Stable
@@ -78,7 +79,7 @@ struct Cfg {
 };
 
 struct Params {
-  void* o;                  // [B,Hq,T,D] bf16
+  void* o;                  // [B,Hq,T,D] bf16 or fp16
   float* lse;               // [B,Hq,T] or null
   const int32_t* key_lens;  // [B] or null
   const int32_t* q_pos;     // [B] key position of query row 0, or null (S - T)
@@ -243,7 +244,8 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   return r;
 }
 
-template <int D>
+// kF16: fp16 inputs and output (else bf16); both use kind::f16 MMAs.
+template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -389,8 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp walks the schedule; one elected lane issues each
     // tcgen05 instruction.  Descriptors are built once per base address and
     // advanced by constants, so every MMA costs only its issue slot.
-    constexpr uint32_t idesc_qk = idesc_bf16(kBM, kBN, false, false);
-    constexpr uint32_t idesc_pv = idesc_bf16(kBM, D, false, true);
+    constexpr uint32_t idesc_qk = idesc_f16kind(kBM, kBN, false, false, kF16);
+    constexpr uint32_t idesc_pv = idesc_f16kind(kBM, D, false, true, kF16);
     const uint64_t dq0 = sdesc_sw128(s_q, 16, 1024);                // Q_0 as the A operand
     const uint64_t dk0 = sdesc_sw128(s_slots, 16, 1024);            // slot 0 as K (K-major B)
     const uint64_t dv0 = sdesc_sw128(s_slots, C::kChunkBytes, 1024);  // slot 0 as V (MN-major B)
@@ -586,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   make_float2(__uint_as_float(sr[c + e]), __uint_as_float(sr[c + e + 1])), sl2x2,
                   negx2);
               const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-              pk[(c + e) >> 1] = pack_bf16x2(pe.x, pe.y);
+              pk[(c + e) >> 1] = pack2<kF16>(pe.x, pe.y);
               if (e == 0) acc0 = __fadd2_rn(acc0, pe);
               else if (e == 2) acc1 = __fadd2_rn(acc1, pe);
               else if (e == 4) acc2 = __fadd2_rn(acc2, pe);
@@ -631,8 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const bool has = row_ok && (l > 0.f);
       const float inv = has ? 1.f / l : 0.f;
-      __nv_bfloat16* orow =
-          reinterpret_cast<__nv_bfloat16*>(p.o) + ((((size_t)it.b * p.Hq + it.h) * p.T) + i) * D;
+      uint16_t* orow =
+          reinterpret_cast<uint16_t*>(p.o) + ((((size_t)it.b * p.Hq + it.h) * p.T) + i) * D;
       if (__any_sync(0xffffffffu, has)) {
         tc_fence_after();
 #pragma unroll
@@ -645,10 +647,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pkd[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            pkd[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv,
+            pkd[e] = pack2<kF16>(__uint_as_float(orr[2 * e]) * inv,
                                  __uint_as_float(orr[2 * e + 1]) * inv);
           if (i < p.T) {
-            __nv_bfloat16* dst = orow + 64 * c;
+            uint16_t* dst = orow + 64 * c;
             if (p.o_align32) {
 #pragma unroll
               for (int v = 0; v < 4; ++v) st_global_v8(dst + 16 * v, pkd + 8 * v);
@@ -675,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int i = it.q0 + t * kBM + r;
       if (i >= p.T) continue;
       const size_t row = ((size_t)it.b * p.Hq + it.h) * p.T + i;
-      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) + row * D);
+      uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.o) + row * D);
 #pragma unroll
       for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
       if (p.lse != nullptr) p.lse[row] = -INFINITY;

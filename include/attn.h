@@ -13,8 +13,9 @@
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream).  A non-zero return means nothing was launched, except
  *    ATTN_ERR_CUDA, which reports a launch error seen right after launching.
- *  - Element types: ATTN_BF16 inputs/outputs with float32 softmax and
- *    accumulation, or ATTN_F32 end to end (no TF32).  LSE is always float32.
+ *  - Element types: ATTN_BF16 or ATTN_F16 inputs/outputs (the output has
+ *    the input type) with float32 softmax and accumulation, or ATTN_F32 end
+ *    to end (no TF32).  LSE is always float32.
  *  - Layouts ("Implementing attention from scratch", Core ideas, Shapes first):
  *      q, o     [B, Hq, T, D]
  *      k, v     [B, Hkv, S, D]
@@ -62,7 +63,7 @@ typedef enum {
   ATTN_ERR_CUDA = 4         /* CUDA runtime/driver error at or before launch */
 } attn_status;
 
-typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
+typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1, ATTN_F16 = 2 } attn_dtype;
 
 /*
  * attn_fwd -- prefill forward: O and (optionally) the per-row LSE.
@@ -86,8 +87,9 @@ typedef enum { ATTN_F32 = 0, ATTN_BF16 = 1 } attn_dtype;
  *   scale    > 0, finite (typically 1/sqrt(D))
  *
  * Supported: B, Hq, Hkv, T, S >= 1, Hq % Hkv == 0.
- *   ATTN_BF16: D in {64, 128}; q, k, v, o 16-byte aligned.  Tensor-core
- *              path (tcgen05 MMAs with TMEM accumulators, TMA tile loads).
+ *   ATTN_BF16, ATTN_F16: D in {64, 128}; q, k, v, o 16-byte aligned.
+ *              Tensor-core path (tcgen05 MMAs with TMEM accumulators, TMA
+ *              tile loads); P is rounded to the input type for P V.
  *   ATTN_F32:  1 <= D <= 256; 4-byte aligned.  Exact float32 path on the
  *              CUDA cores (FFMA, accurate expf), no TF32.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED or
@@ -166,8 +168,9 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int T);
  *                            (q_pos NULL = bottom-right, S - T)
  *   workspace   >= attn_bwd_workspace_size(B, Hq, T) bytes, 16-byte aligned
  *
- * Supported: ATTN_BF16 with D in {64, 128} (tcgen05 tensor cores, fp32
- * accumulation; P and dS are rounded to bf16 for the products); all
+ * Supported: ATTN_BF16 or ATTN_F16 with D in {64, 128} (tcgen05 tensor
+ * cores, fp32 accumulation; P and dS are rounded to the input type for the
+ * products); all
  * pointers 16-byte aligned (lse, key_lens, q_pos: 4).  ATTN_F32 returns
  * ATTN_ERR_UNSUPPORTED.  No atomics: results do not depend on scheduling.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
@@ -210,8 +213,8 @@ ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int S_max, int D);
  *   workspace device scratch of >= attn_decode_workspace_size(B,Hq,S_max,D)
  *             bytes, 16-byte aligned; contents need no initialisation.
  *
- * Supported: dtype ATTN_BF16 or ATTN_F32; D in {64, 128}; Hq % Hkv == 0 and
- * Hq / Hkv <= 16; q, caches, o 16-byte aligned.
+ * Supported: dtype ATTN_BF16, ATTN_F16 or ATTN_F32; D in {64, 128};
+ * Hq % Hkv == 0 and Hq / Hkv <= 16; q, caches, o 16-byte aligned.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
  * ATTN_ERR_WORKSPACE or ATTN_ERR_CUDA.
  */
@@ -270,8 +273,8 @@ ATTN_API int attn_decode_noalloc(const void* q, const void* kcache, const void* 
  *                                           NOT written and bit 0 is OR-ed
  *                                           into *dev_status)
  *
- * Supported: dtype ATTN_BF16 or ATTN_F32; D >= 1 with D * element size a
- * multiple of 16 bytes; all tensor pointers 16-byte aligned.
+ * Supported: dtype ATTN_BF16, ATTN_F16 or ATTN_F32; D >= 1 with D *
+ * element size a multiple of 16 bytes; all tensor pointers 16-byte aligned.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG or ATTN_ERR_CUDA.
  */
 ATTN_API int kv_cache_append(void* kcache, void* vcache, const void* k_new,

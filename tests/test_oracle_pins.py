@@ -595,3 +595,21 @@ def test_clean_copy_passes_all_pins():
 def test_pins_catch_planted_mistakes(mistake):
     caught_by = _fails_some_pin(_mutant(mistake))
     assert caught_by is not None, f"no pin catches the planted mistake {mistake!r}"
+
+
+def test_f16_inputs_are_widened_exactly():
+    """fp16 inputs reach the oracle as their exact float64 values: the C
+    oracle on float16 arrays equals the C oracle on the same values stored
+    as float64, and both equal the NumPy twin."""
+    r = _rng(77)
+    q, k, v = (r.standard_normal(s).astype(np.float16) for s in
+               ((2, 2, 9, 8), (2, 1, 11, 8), (2, 1, 11, 8)))
+    a = oracle.attn_fwd(q, k, v, causal=True, nthreads=1)
+    b = oracle.attn_fwd(q.astype(np.float64), k.astype(np.float64), v.astype(np.float64),
+                        causal=True, nthreads=1)
+    c = oracle.attn_fwd_np(q, k, v, causal=True)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert np.allclose(a[0], c[0], atol=ATOL) and np.allclose(a[1], c[1], atol=ATOL)
+    # every float16 value is a float64 value exactly (11-bit significand)
+    x = np.arange(-65504, 65505, 97, dtype=np.float64).astype(np.float16)
+    assert np.array_equal(x.astype(np.float64).astype(np.float16), x)

@@ -70,7 +70,7 @@ WORKLOADS = {
                 S=4096, causal=True, lens=(2048, 4096)),
 }
 
-_DT = {"f32": torch.float32, "bf16": torch.bfloat16}
+_DT = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}
 
 
 def lengths(seed: int, lo: int, hi: int, B: int) -> np.ndarray:
@@ -150,7 +150,8 @@ def workload_inputs(wid: int, device="cpu", batch: int | None = None):
 
 
 def to_numpy_exact(t: torch.Tensor):
-    """(array, is_bf16): float32/float64 as is, bf16 as raw uint16 bits."""
+    """(array, is_bf16): float16/float32/float64 as is (NumPy widens them
+    exactly), bf16 as raw uint16 bits."""
     t = t.detach().to("cpu").contiguous()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16), True
