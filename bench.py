@@ -208,6 +208,11 @@ class ClockSampler:
 
 # -------------------------------------------------------------- workloads
 
+def workloads_kind(wid):
+    import workloads
+    return workloads.WORKLOADS[wid].kind
+
+
 def prefill_flops(w, key_lens=None):
     """Algorithmic FLOPs of one prefill forward: 4*B*H*T*S*D for full
     attention, the unmasked half 2*B*H*T*S*D for causal, and 2*H*D*sum(L^2)
@@ -229,8 +234,10 @@ def decode_flops(Hq, D, kv_lens):
     return 4.0 * Hq * D * float(sum(int(x) for x in kv_lens))
 
 
-def build_case(wid, device, batch=None):
-    """Device tensors for one step of workload `wid` and its bookkeeping."""
+def build_case(wid, device, batch=None, backward=False):
+    """Device tensors for one step of workload `wid` and its bookkeeping.
+    With `backward`, the step is the backward pass of the prefill (its O and
+    LSE computed once, outside the timed region)."""
     import torch
     import workloads
     w = workloads.workload(wid, batch)
@@ -242,6 +249,21 @@ def build_case(wid, device, batch=None):
         case["lse"] = torch.empty(w.B, w.Hq, w.T, device=device, dtype=torch.float32)
         kl = None if x["key_lens"] is None else x["key_lens"].cpu().numpy()
         case["flops"] = prefill_flops(w, kl)
+        if backward:
+            import exact_tiled_attention_49_b300 as E
+            scale = 1.0 / math.sqrt(w.D)
+            o, lse = E.attn_fwd(x["q"], x["k"], x["v"], causal=w.causal,
+                                key_lens=x["key_lens"], scale=scale)
+            g = torch.Generator(device=device).manual_seed(100 + wid)
+            case["bwd"] = {
+                "o": o, "lse": lse,
+                "do": torch.randn(x["q"].shape, generator=g, device=device).to(x["q"].dtype),
+                "ws": torch.empty(E.attn_bwd_workspace_size(w.B, w.Hq, w.T), dtype=torch.uint8,
+                                  device=device),
+                "dq": torch.empty_like(x["q"]), "dk": torch.empty_like(x["k"]),
+                "dv": torch.empty_like(x["v"])}
+            case["flops"] = 2.5 * prefill_flops(w, kl)
+            return case
         if wid == 2:
             # the next generation step for the same batch: cache = prompt K/V
             s_max = w.S + 1
@@ -287,6 +309,13 @@ def step_groups(c):
     w = c["w"]
     scale = 1.0 / math.sqrt(w.D)
     groups = []
+    if "bwd" in c:
+        bw = c["bwd"]
+        groups.append(("prefill", lambda: E.attn_bwd(
+            c["q"], c["k"], c["v"], bw["o"], bw["do"], bw["lse"], causal=w.causal,
+            key_lens=c["key_lens"], scale=scale, dq=bw["dq"], dk=bw["dk"], dv=bw["dv"],
+            workspace=bw["ws"])))
+        return groups
     if w.kind == "prefill":
         groups.append(("prefill", lambda: E.attn_fwd(
             c["q"], c["k"], c["v"], o=c["o"], lse=c["lse"], causal=w.causal,
@@ -465,6 +494,32 @@ def run_e2e(E, c, steps, device):
     the step's inputs, the step, D2H copy of its outputs, all timed."""
     import torch
     w = c["w"]
+    if "bwd" in c:
+        # backward: inputs q, k, v, dO, O, LSE; results dQ, dK, dV
+        bw = c["bwd"]
+        dev_in = {"q": c["q"], "k": c["k"], "v": c["v"], "do": bw["do"], "o": bw["o"],
+                  "lse": bw["lse"]}
+        host_in = {n: t.cpu().pin_memory() for n, t in dev_in.items()}
+        outs = [(torch.empty(bw[n].shape, dtype=bw[n].dtype).pin_memory(), bw[n])
+                for n in ("dq", "dk", "dv")]
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(h.numel() * h.element_size() for h, _ in outs)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        total = 0.0
+        for _ in range(steps):
+            flush.zero_()
+            s0.record()
+            for n, t in dev_in.items():
+                t.copy_(host_in[n], non_blocking=True)
+            run_step(E, c)
+            for h, dv in outs:
+                h.copy_(dv, non_blocking=True)
+            s1.record()
+            s1.synchronize()
+            total += s0.elapsed_time(s1)
+        return total / steps, h2d, d2h
     names_in = ["q", "k", "v"] if w.kind == "prefill" else ["q", "k_new", "v_new"]
     host_in = {n: c[n].cpu().pin_memory() for n in names_in}
     host_o = torch.empty(c["o"].shape, dtype=c["o"].dtype).pin_memory()
@@ -559,6 +614,45 @@ def cpu_baseline(wid, budget_s=12.0, seed=0):
         f"{reps} decode steps of an 8-sequence batch of {w.name}, {t_used:.1f} s"
 
 
+def cpu_baseline_bwd(wid, budget_s=12.0, seed=0):
+    """Time the float64 oracle's backward on the host over a bounded sample:
+    whole (b, kv-head group) slices of the prefill workload, one at a time.
+    Counts 2.5x the forward's visible-key FLOPs, the GPU line's unit."""
+    import numpy as np
+    import oracle
+    import workloads
+    w = workloads.WORKLOADS[wid]
+    G = w.Hq // w.Hkv
+    # the dense float64 matrices of a 32k x 32k slice would take 8.6 GB each:
+    # long sequences are sampled as their first 4096 x 4096 causal block
+    T, S = min(w.T, 4096), min(w.S, 4096)
+    x = workloads.prefill_inputs(1, G, 1, T, S, w.D, w.dtype, seed=wid, q_scale=w.q_scale)
+    q, k, v = (workloads.to_numpy_exact(x[n])[0] for n in ("q", "k", "v"))
+    rng = np.random.default_rng(seed)
+    do = rng.standard_normal(q.shape)
+    lo_hi = None if w.lens is None else (min(w.lens[0], S), min(w.lens[1], S))
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except ImportError:
+        cores = 1
+    t_used, flops, slices = 0.0, 0.0, 0
+    while t_used < budget_s:
+        L = S if lo_hi is None else int(rng.integers(lo_hi[0], lo_hi[1] + 1))
+        t0 = time.perf_counter()
+        oracle.attn_bwd_np(q, k, v, do, causal=w.causal, key_lens=np.array([L]),
+                           scale=1 / math.sqrt(w.D), bf16=True)
+        t_used += time.perf_counter() - t0
+        i = np.arange(T)
+        vis = np.minimum(L, i + (S - T) + 1) if w.causal else np.full(T, L)
+        vis = np.where(i + (S - T) < L, np.maximum(vis, 0), 0)
+        flops += 2.5 * float((4.0 * w.D * vis).sum()) * G
+        slices += 1
+    return flops / t_used / 1e12, "TFLOPS", cores, \
+        (f"{slices} single (b, kv-head group of {G}) backward slices, T={T} S={S}, "
+         f"of {w.name}, {t_used:.1f} s")
+
+
 # ------------------------------------------------------------------- arms
 
 def bench_ours(args):
@@ -577,7 +671,9 @@ def bench_ours(args):
     import exact_tiled_attention_49_b300 as E
     E.load()
     peaks = load_peaks()
-    c = build_case(args.workload, device, args.batch)
+    if args.backward and workloads_kind(args.workload) != "prefill":
+        raise SystemExit("--backward needs a prefill workload (2, 3 or 5)")
+    c = build_case(args.workload, device, args.batch, backward=args.backward)
     w = c["w"]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     for _ in range(args.warmup):
@@ -609,10 +705,12 @@ def bench_ours(args):
     if w.kind == "prefill":
         out["value"] = total_flops / (ms_per_step * 1e-3) / 1e12
         out["unit"] = "TFLOPS"
-        achieved = (prefill_flops(w, None if c["key_lens"] is None else c["key_lens"].cpu().numpy())
-                    / (kern_ms["prefill"] * 1e-3) / 1e12)
+        achieved = (c["flops"] if "bwd" in c else
+                    prefill_flops(w, None if c["key_lens"] is None else c["key_lens"].cpu().numpy())
+                    ) / (kern_ms["prefill"] * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
-        out["roofline"] = {"kernel": "fwd_bf16_tc_kernel", "bound": "tensor",
+        out["roofline"] = {"kernel": ("bwd_delta_kernel+bwd_dq_kernel+bwd_dkdv_kernel"
+                                      if "bwd" in c else "fwd_bf16_tc_kernel"), "bound": "tensor",
                            "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                            "frac": achieved / peak,
                            "traffic": profiled_traffic(args.workload) if args.batch is None else None,
@@ -633,7 +731,8 @@ def bench_ours(args):
                            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                            "traffic": profiled_traffic(args.workload) if args.batch is None else None,
                            "peak_source": peaks["source"] + " HBM copy"}
-    cfg = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+    cfg = {"workload": ("backward (dQ, dK, dV, 2.5x the forward's FLOPs) of: " + w.name
+                        if "bwd" in c else w.name), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
            "l2": "flushed between steps (256 MiB write, outside the timed events)",
            "timing": "CUDA events around CUDA-graph replays of each kernel group of the step",
            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
@@ -662,7 +761,8 @@ def bench_ours(args):
                                                  max(3, min(K, 10)), peaks)
 
     if rank == 0 and not args.no_cpu_baseline:
-        v, unit, cores, sample = cpu_baseline(args.workload, budget_s=args.cpu_budget)
+        fn = cpu_baseline_bwd if args.backward else cpu_baseline
+        v, unit, cores, sample = fn(args.workload, budget_s=args.cpu_budget)
         out["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
                                "sample": sample}
     if rank == 0:
@@ -711,6 +811,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (dQ, dK, dV) of the prefill workload instead")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip timing the other benchmark workloads")
     ap.add_argument("--batch", type=int, default=None,
