@@ -236,11 +236,13 @@ int launch_bwd_tc(const attn::tcbwd::Params& p0, const void* q, const void* k, c
   bwd_delta_kernel<kF16><<<blocks, 256, 0, st>>>(p0, rows);
   int rc = launch_status();
   if (rc != ATTN_OK) return rc;
-  kdq<<<dim3(p0.n_qtiles, p0.Hq, p0.B), kThreads, Cfg<D>::kSmemAlloc, st>>>(tq, tdo, tk, tv, p0);
+  // x = (batch, head) varies fastest, so the heaviest tiles of every head
+  // are dispatched first
+  kdq<<<dim3(p0.B * p0.Hq, p0.n_qtiles), kThreads, Cfg<D>::kSmemAlloc, st>>>(tq, tdo, tk, tv, p0);
   rc = launch_status();
   if (rc != ATTN_OK) return rc;
-  kdkdv<<<dim3(p0.n_ktiles, p0.Hkv, p0.B), kThreads, Cfg<D>::kSmemAlloc, st>>>(tq, tdo, tk, tv,
-                                                                              p0);
+  kdkdv<<<dim3(p0.B * p0.Hkv, p0.n_ktiles), kThreads, Cfg<D>::kSmemAlloc, st>>>(tq, tdo, tk, tv,
+                                                                               p0);
   return launch_status();
 }
 
@@ -374,6 +376,8 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   if (dtype != ATTN_BF16 && dtype != ATTN_F16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
   if (dtype == ATTN_F32 || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
   if (B > 65535 || Hq > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * Hq > 0x7fffffffll || (T + 127) / 128 > 65535 || (S + 127) / 128 > 65535)
+    return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned4(lse) ||
       (key_lens != nullptr && !aligned4(key_lens)) || (q_pos != nullptr && !aligned4(q_pos)))

@@ -108,19 +108,38 @@ struct Cfg {
   // dK/dV kernel: per elementwise warp, the 128 LSE and delta values of the
   // current query tile (4 warps x 2 x 128 floats)
   static constexpr uint32_t kOffBars = kOffStats + 4 * 2 * kBM * 4;
-  // barriers: fixed_full, ring_full[kStages], ring_empty[kStages], mm_full
-  // (S and dP done), p_full (dS / P^T and dS^T in TMEM), acc_full, drain,
-  // tail (dQ kernel: the K/V tile that straddles the valid key length)
-  static constexpr int kNumBars = 1 + 2 * kStages + 5;
+  // barriers: fixed_full, ring_full[kStages], ring_empty[kStages], mm[2]
+  // (S and dP of a 64-column half done), pp[2] (that half's packed P / dS
+  // in TMEM), acc_full, drain, tail (dQ kernel: the K/V tile that straddles
+  // the valid key length)
+  static constexpr int kNumBars = 1 + 2 * kStages + 7;
   static constexpr uint32_t kOffMisc = kOffBars + 8 * kNumBars;
   static constexpr uint32_t kBytes = kOffMisc + 16;
   static constexpr size_t kSmemAlloc = kBytes + 1024;
 };
 
+// Both kernels split every 128x128 product tile into two 64-column halves
+// with their own TMEM columns: half h holds S (or S^T) at 128h and dP (or
+// dP^T) at 128h + 64.  The MMA warp issues S/dP of one half while the
+// elementwise warps turn the other half into packed bf16 P / dS (written
+// back over the first 32 columns of S and dP), so the tensor core and the
+// CUDA cores overlap:
+//
+//   MMA:  SdP(u,0) SdP(u,1) | acc(u,0) SdP(u+1,0) | acc(u,1) SdP(u+1,1) | ...
+//   ALU:        half(u,0)   |   half(u,1)         |   half(u+1,0)       | ...
+//
+// The accumulating products read a half's packed operand before the next
+// S/dP of that half overwrites its columns: tcgen05.mma operations issued
+// by one thread execute in order.
+constexpr int kHalf = 64;
+__device__ __forceinline__ constexpr uint32_t col_s(int h) { return 128u * h; }
+__device__ __forceinline__ constexpr uint32_t col_dp(int h) { return 128u * h + 64u; }
+constexpr uint32_t kColAcc = 256;
+
 // ------------------------------------------------------------- dQ kernel
 //
-// TMEM: S at column 0 (dS packed over its first 64 columns), dP at 128,
-// dQ at 256.
+// Grid: x = (batch, query head), y = query tile, heaviest causal tiles first
+// (y = 0 is the last query tile).  TMEM: S/dP halves at 0..255, dQ at 256.
 template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -128,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, Params p) {
   using C = Cfg<D>;
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kTmemCols = 512;
+  constexpr uint32_t kColDQ = kColAcc, kTmemCols = 512;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -139,15 +158,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_fixed = bars;
   auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
   auto bar_empty = [&](int s) { return bars + 8u * (1 + C::kStages + s); };
-  const uint32_t bar_mm = bars + 8u * (1 + 2 * C::kStages);
-  const uint32_t bar_p = bar_mm + 8, bar_acc = bar_p + 8, bar_drain = bar_acc + 8;
-  const uint32_t bar_tail = bar_drain + 8;
+  const uint32_t bar_mm0 = bars + 8u * (1 + 2 * C::kStages);  // mm[h] = bar_mm0 + 8h
+  const uint32_t bar_pp0 = bar_mm0 + 16;                       // pp[h] = bar_pp0 + 8h
+  const uint32_t bar_acc = bar_pp0 + 16, bar_drain = bar_acc + 8, bar_tail = bar_drain + 8;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = p.n_qtiles - 1 - (int)blockIdx.x;  // heaviest causal tiles first
-  const int h = blockIdx.y, b = blockIdx.z;
+  const int qt = p.n_qtiles - 1 - (int)blockIdx.y;
+  const int b = (int)blockIdx.x / p.Hq, h = (int)blockIdx.x % p.Hq;
   const int g = h / (p.Hq / p.Hkv);
   const int q0 = qt * kBM;
   const int L = key_bound(p, b);
@@ -165,8 +184,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_full(s), 1);
       mbar_init(bar_empty(s), 1);
     }
-    mbar_init(bar_mm, 1);
-    mbar_init(bar_p, 4 * 32);
+    mbar_init(bar_mm0, 1);
+    mbar_init(bar_mm0 + 8, 1);
+    mbar_init(bar_pp0, 4 * 32);
+    mbar_init(bar_pp0 + 8, 4 * 32);
     mbar_init(bar_acc, 1);
     mbar_init(bar_drain, 1);
     mbar_init(bar_tail, 1);
@@ -243,55 +264,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc_ss = idesc_f16kind(kBM, kBM, false, false, kF16);   // M=N=128, K-major
+    constexpr uint32_t idesc_s = idesc_f16kind(kBM, kHalf, false, false, kF16);  // M=128, N=64, K-major
     constexpr uint32_t idesc_ts = idesc_f16kind(kBM, D, false, true, kF16);      // B MN-major, N = D
     const uint64_t dq_a = sdesc_sw128(s_q, 16, 1024), ddo_a = sdesc_sw128(s_do, 16, 1024);
     const uint64_t dk0 = sdesc_sw128(s_ring, 16, 1024);
     const uint64_t dkmn0 = sdesc_sw128(s_ring, C::kChunkBytes, 1024);
     bool ok = n > 0 && __all_sync(0xffffffffu, mbar_wait(bar_fixed, 0, 3, abort_flag));
-    auto issue_s_dp = [&](int s) {
-      const uint64_t dk = dk0 + (uint64_t)((2 * s * C::kTileBytes) >> 4);
-      const uint64_t dv = dk0 + (uint64_t)(((2 * s + 1) * C::kTileBytes) >> 4);
+    // S_h = Q K_j[64h, 64h + 64)^T and dP_h = dO V_j[64h, 64h + 64)^T: the
+    // B operand starts 64 rows (8 swizzle atoms) into each 128-row chunk.
+    auto issue_sdp = [&](int s, int hh) {
+      const uint64_t rows = (uint64_t)((hh * kHalf * 128) >> 4);
+      const uint64_t dk = dk0 + (uint64_t)((2 * s * C::kTileBytes) >> 4) + rows;
+      const uint64_t dv = dk0 + (uint64_t)(((2 * s + 1) * C::kTileBytes) >> 4) + rows;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t ko = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-        umma_ss_elect(tmem + kColS, dq_a + ko, dk + ko, idesc_ss, kk > 0);
+        umma_ss_elect(tmem + col_s(hh), dq_a + ko, dk + ko, idesc_s, kk > 0);
       }
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t ko = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-        umma_ss_elect(tmem + kColDP, ddo_a + ko, dv + ko, idesc_ss, kk > 0);
+        umma_ss_elect(tmem + col_dp(hh), ddo_a + ko, dv + ko, idesc_s, kk > 0);
       }
-      umma_commit_elect(bar_mm);
+      umma_commit_elect(bar_mm0 + 8u * hh);
+    };
+    // dQ += dS_h K_j[64h, 64h + 64): A = packed dS_h in TMEM, K = 64 keys
+    auto issue_dq = [&](int s, int hh, bool first) {
+      const uint64_t dkmn = dkmn0 + (uint64_t)((2 * s * C::kTileBytes) >> 4) + (uint64_t)(hh * 4 * 128);
+#pragma unroll
+      for (int kk = 0; kk < kHalf / 16; ++kk)
+        umma_ts_elect(tmem + kColDQ, tmem + col_s(hh) + kk * 8, dkmn + (uint64_t)(kk * 128),
+                      idesc_ts, (!first || kk > 0) ? 1u : 0u);
     };
     if (ok) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar_full(0), 0, 4, abort_flag));
       if (ok) {
         tc_fence_after();
-        issue_s_dp(0);
+        issue_sdp(0, 0);
+        issue_sdp(0, 1);
       }
     }
     for (int j = 0; ok && j < n; ++j) {
-      const int s = j % C::kStages;
-      // dS_j is in TMEM (packed over the S columns)
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_p, j & 1, 5, abort_flag)))) break;
+      const int s = j % C::kStages, s1 = (j + 1) % C::kStages;
+      const bool more = j + 1 < n;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_pp0, j & 1, 5, abort_flag)))) break;
       tc_fence_after();
-      const uint64_t dkmn = dkmn0 + (uint64_t)((2 * s * C::kTileBytes) >> 4);
-#pragma unroll
-      for (int kk = 0; kk < kBM / 16; ++kk)
-        umma_ts_elect(tmem + kColDQ, tmem + kColS + kk * 8, dkmn + (uint64_t)(kk * 128), idesc_ts,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-      umma_commit_elect(bar_empty(s));
-      if (j + 1 < n) {
-        const int s1 = (j + 1) % C::kStages;
+      issue_dq(s, 0, j == 0);
+      if (more) {
         if (!(ok = __all_sync(0xffffffffu,
                               mbar_wait(bar_full(s1), ((j + 1) / C::kStages) & 1, 4, abort_flag))))
           break;
         tc_fence_after();
-        issue_s_dp(s1);
-      } else {
-        umma_commit_elect(bar_acc);
+        issue_sdp(s1, 0);
       }
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_pp0 + 8, j & 1, 5, abort_flag)))) break;
+      tc_fence_after();
+      issue_dq(s, 1, false);
+      umma_commit_elect(bar_empty(s));
+      if (more) issue_sdp(s1, 1);
+      else umma_commit_elect(bar_acc);
     }
     umma_commit_elect(bar_drain);
     mbar_wait(bar_drain, 0, 6);
@@ -303,45 +334,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pos = i + off;
     const bool row_ok = (i < p.T) && (pos < L);
     const int lim = !row_ok ? 0 : (p.causal ? min(L, pos + 1) : L);  // visible keys [0, lim)
+    const int lim_warp = __reduce_min_sync(0xffffffffu, lim);
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     const size_t row = ((size_t)b * p.Hq + h) * p.T + i;
     const float lse2 = row_ok ? p.lse[row] * 1.4426950408889634f : 0.f;
     const float dlt = row_ok ? p.delta[row] : 0.f;
-    const float sl2 = p.scale_log2;
+    const float2 sl2x2 = make_float2(p.scale_log2, p.scale_log2);
+    const float2 nl2 = make_float2(-lse2, -lse2);
+    const float2 ndl2 = make_float2(-dlt, -dlt);
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_mm, j & 1, 7, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
-      const int k0 = j * kBM;
-      // 32 columns at a time: P = exp2(s * scale*log2e - lse*log2e) on
-      // visible keys, dS = P (dP - delta); dS packed to bf16 over the first
-      // 64 columns of S (chunk c goes to columns 16c.., all of which have
-      // been read by then).
+    for (int j = 0; ok && j < n; ++j) {
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_mm0 + 8u * hh, j & 1, 7, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const int kb = j * kBM + hh * kHalf;  // first key of the half
+        // Every key of the half visible to every row of the warp: no masks.
+        const bool dense = kb + kHalf <= lim_warp;
+        // 32 columns at a time: P = exp2(s * scale*log2e - lse*log2e) on
+        // visible keys, dS = P (dP - delta), packed to bf16 over the first
+        // 32 columns of the half's S (chunk c goes to columns 16c.., all of
+        // which have been read by then).
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32], dp[32];
-        tmem_ld32(lane_base + kColS + 32 * c, sr);
-        tmem_ld32(lane_base + kColDP + 32 * c, dp);
-        tmem_wait_ld32(sr);
-        tmem_wait_ld32(dp);
-        uint32_t pk[16];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sr[32], dp[32];
+          tmem_ld32(lane_base + col_s(hh) + 32 * c, sr);
+          tmem_ld32(lane_base + col_dp(hh) + 32 * c, dp);
+          tmem_wait_ld32(sr);
+          tmem_wait_ld32(dp);
+          uint32_t pk[16];
+          if (dense) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int kj = k0 + 32 * c + e;
-          // selects, not products: hidden entries may hold NaN (keys past
-          // the valid length), and 0 * NaN would be NaN
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[e]), sl2, -lse2));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), sl2, -lse2));
-          const float d0 = (kj < lim) ? p0 * (__uint_as_float(dp[e]) - dlt) : 0.f;
-          const float d1 = (kj + 1 < lim) ? p1 * (__uint_as_float(dp[e + 1]) - dlt) : 0.f;
-          pk[e >> 1] = pack2<kF16>(d0, d1);
+            for (int e = 0; e < 32; e += 2) {
+              const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                          sl2x2, nl2);
+              const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              const float2 d = __fadd2_rn(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                          ndl2);
+              const float2 ds = __fmul2_rn(pe, d);
+              pk[e >> 1] = pack2<kF16>(ds.x, ds.y);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const int kj = kb + 32 * c + e;
+              // selects, not products: hidden entries may hold NaN (keys past
+              // the valid length), and 0 * NaN would be NaN
+              const float p0 = ex2_approx(fmaf(__uint_as_float(sr[e]), sl2x2.x, -lse2));
+              const float p1 = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), sl2x2.x, -lse2));
+              const float d0 = (kj < lim) ? p0 * (__uint_as_float(dp[e]) - dlt) : 0.f;
+              const float d1 = (kj + 1 < lim) ? p1 * (__uint_as_float(dp[e + 1]) - dlt) : 0.f;
+              pk[e >> 1] = pack2<kF16>(d0, d1);
+            }
+          }
+          tmem_st16(lane_base + col_s(hh) + 16 * c, pk);
         }
-        tmem_st16(lane_base + kColS + 16 * c, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_pp0 + 8u * hh);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_p);
     }
     // ------------------------------------------------------------ epilogue
     if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_acc, 0, 8, abort_flag));
@@ -376,14 +428,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 // ----------------------------------------------------------- dK/dV kernel
 //
-// TMEM: S^T at column 0 (P^T packed over its first 64 columns), dP^T at 128
-// (dS^T packed over its first 64), dV at 256, dK at 256 + D.
+// Grid: x = (batch, kv head), y = key tile (the first key tiles are the
+// heaviest under a causal mask).  TMEM: S^T/dP^T halves at 0..255 (a half =
+// 64 query columns; P^T and dS^T packed over the first 32 columns of each),
+// dV at 256, dK at 256 + D.
 template <int D, bool kF16>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -391,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, Params p) {
   using C = Cfg<D>;
-  constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+  constexpr uint32_t kColDV = kColAcc, kColDK = kColAcc + D;
   constexpr uint32_t kTmemCols = 512;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -404,14 +458,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_fixed = bars;
   auto bar_full = [&](int s) { return bars + 8u * (1 + s); };
   auto bar_empty = [&](int s) { return bars + 8u * (1 + C::kStages + s); };
-  const uint32_t bar_mm = bars + 8u * (1 + 2 * C::kStages);
-  const uint32_t bar_p = bar_mm + 8, bar_acc = bar_p + 8, bar_drain = bar_acc + 8;
+  const uint32_t bar_mm0 = bars + 8u * (1 + 2 * C::kStages);
+  const uint32_t bar_pp0 = bar_mm0 + 16;
+  const uint32_t bar_acc = bar_pp0 + 16, bar_drain = bar_acc + 8;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int kt = (int)blockIdx.x;  // first key tiles are the heaviest under a causal mask
-  const int g = blockIdx.y, b = blockIdx.z;
+  const int kt = (int)blockIdx.y;
+  const int b = (int)blockIdx.x / p.Hkv, g = (int)blockIdx.x % p.Hkv;
   const int G = p.Hq / p.Hkv;
   const int k0 = kt * kBM;
   const int L = key_bound(p, b);
@@ -434,8 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_full(s), 1);
       mbar_init(bar_empty(s), 1);
     }
-    mbar_init(bar_mm, 1);
-    mbar_init(bar_p, 4 * 32);
+    mbar_init(bar_mm0, 1);
+    mbar_init(bar_mm0 + 8, 1);
+    mbar_init(bar_pp0, 4 * 32);
+    mbar_init(bar_pp0 + 8, 4 * 32);
     mbar_init(bar_acc, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -483,59 +540,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc_ss = idesc_f16kind(kBM, kBM, false, false, kF16);
+    constexpr uint32_t idesc_s = idesc_f16kind(kBM, kHalf, false, false, kF16);
     constexpr uint32_t idesc_ts = idesc_f16kind(kBM, D, false, true, kF16);
     const uint64_t dk_a = sdesc_sw128(s_k, 16, 1024), dv_a = sdesc_sw128(s_v, 16, 1024);
     const uint64_t dr0 = sdesc_sw128(s_ring, 16, 1024);
     const uint64_t drmn0 = sdesc_sw128(s_ring, C::kChunkBytes, 1024);
     bool ok = n > 0 && __all_sync(0xffffffffu, mbar_wait(bar_fixed, 0, 3, abort_flag));
-    auto issue_s_dp = [&](int s) {
-      const uint64_t dq_ = dr0 + (uint64_t)((2 * s * C::kTileBytes) >> 4);
-      const uint64_t ddo = dr0 + (uint64_t)(((2 * s + 1) * C::kTileBytes) >> 4);
+    // S^T_h = K Q[64h, 64h + 64)^T and dP^T_h = V dO[64h, 64h + 64)^T
+    auto issue_sdp = [&](int s, int hh) {
+      const uint64_t rows = (uint64_t)((hh * kHalf * 128) >> 4);
+      const uint64_t dq_ = dr0 + (uint64_t)((2 * s * C::kTileBytes) >> 4) + rows;
+      const uint64_t ddo = dr0 + (uint64_t)(((2 * s + 1) * C::kTileBytes) >> 4) + rows;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t ko = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-        umma_ss_elect(tmem + kColS, dk_a + ko, dq_ + ko, idesc_ss, kk > 0);   // S^T = K Q^T
+        umma_ss_elect(tmem + col_s(hh), dk_a + ko, dq_ + ko, idesc_s, kk > 0);
       }
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t ko = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-        umma_ss_elect(tmem + kColDP, dv_a + ko, ddo + ko, idesc_ss, kk > 0);  // dP^T = V dO^T
+        umma_ss_elect(tmem + col_dp(hh), dv_a + ko, ddo + ko, idesc_s, kk > 0);
       }
-      umma_commit_elect(bar_mm);
+      umma_commit_elect(bar_mm0 + 8u * hh);
+    };
+    // dV += P^T_h dO[64h..] and dK += dS^T_h Q[64h..], K = 64 queries
+    auto issue_acc = [&](int s, int hh, bool first) {
+      const uint64_t half = (uint64_t)(hh * 4 * 128);
+      const uint64_t dqmn = drmn0 + (uint64_t)((2 * s * C::kTileBytes) >> 4) + half;
+      const uint64_t ddomn = drmn0 + (uint64_t)(((2 * s + 1) * C::kTileBytes) >> 4) + half;
+#pragma unroll
+      for (int kk = 0; kk < kHalf / 16; ++kk)
+        umma_ts_elect(tmem + kColDV, tmem + col_s(hh) + kk * 8, ddomn + (uint64_t)(kk * 128),
+                      idesc_ts, (!first || kk > 0) ? 1u : 0u);
+#pragma unroll
+      for (int kk = 0; kk < kHalf / 16; ++kk)
+        umma_ts_elect(tmem + kColDK, tmem + col_dp(hh) + kk * 8, dqmn + (uint64_t)(kk * 128),
+                      idesc_ts, (!first || kk > 0) ? 1u : 0u);
     };
     if (ok) {
       ok = __all_sync(0xffffffffu, mbar_wait(bar_full(0), 0, 4, abort_flag));
       if (ok) {
         tc_fence_after();
-        issue_s_dp(0);
+        issue_sdp(0, 0);
+        issue_sdp(0, 1);
       }
     }
     for (int u = 0; ok && u < n; ++u) {
-      const int s = u % C::kStages;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_p, u & 1, 5, abort_flag)))) break;
+      const int s = u % C::kStages, s1 = (u + 1) % C::kStages;
+      const bool more = u + 1 < n;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_pp0, u & 1, 5, abort_flag)))) break;
       tc_fence_after();
-      const uint64_t dqmn = drmn0 + (uint64_t)((2 * s * C::kTileBytes) >> 4);
-      const uint64_t ddomn = drmn0 + (uint64_t)(((2 * s + 1) * C::kTileBytes) >> 4);
-#pragma unroll
-      for (int kk = 0; kk < kBM / 16; ++kk)  // dV += P^T dO
-        umma_ts_elect(tmem + kColDV, tmem + kColS + kk * 8, ddomn + (uint64_t)(kk * 128), idesc_ts,
-                      (u > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-      for (int kk = 0; kk < kBM / 16; ++kk)  // dK += dS^T Q
-        umma_ts_elect(tmem + kColDK, tmem + kColDP + kk * 8, dqmn + (uint64_t)(kk * 128), idesc_ts,
-                      (u > 0 || kk > 0) ? 1u : 0u);
-      umma_commit_elect(bar_empty(s));
-      if (u + 1 < n) {
-        const int s1 = (u + 1) % C::kStages;
+      issue_acc(s, 0, u == 0);
+      if (more) {
         if (!(ok = __all_sync(0xffffffffu,
                               mbar_wait(bar_full(s1), ((u + 1) / C::kStages) & 1, 4, abort_flag))))
           break;
         tc_fence_after();
-        issue_s_dp(s1);
-      } else {
-        umma_commit_elect(bar_acc);
+        issue_sdp(s1, 0);
       }
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar_pp0 + 8, u & 1, 5, abort_flag)))) break;
+      tc_fence_after();
+      issue_acc(s, 1, false);
+      umma_commit_elect(bar_empty(s));
+      if (more) issue_sdp(s1, 1);
+      else umma_commit_elect(bar_acc);
     }
     umma_commit_elect(bar_drain);
     mbar_wait(bar_drain, 0, 6);
@@ -548,59 +616,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* st_lse = stats + warp * 2 * kBM;  // this warp's copy of the tile statistics
     float* st_dlt = st_lse + kBM;
     const float sl2 = p.scale_log2;
-    bool ok = true;
-    for (int u = 0; u < n; ++u) {
+    const float2 sl2x2 = make_float2(sl2, sl2);
+    const bool key_ok = kj < L;
+    const bool keys_ok = __all_sync(0xffffffffu, key_ok);
+    const int kj_warp_max = k0 + warp * 32 + 31;
+    // LSE*log2e and delta of item u's 128 query rows, 4 per lane; rows that
+    // are past T or padded get lse = +inf (P = 0).  Loaded one item ahead.
+    float nl[4], nd[4];
+    auto fetch = [&](int u) {
       const int hq = g * G + u / n_tiles_per_head;
       const int q0 = (i_lo + u % n_tiles_per_head) * kBM;
-      // LSE*log2e and delta of the tile's 128 query rows; rows that are past
-      // T or padded get lse = +inf (P = 0).
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = q0 + lane + 32 * e;
+        const bool valid = i < p.T && i + off < L;
+        const size_t row = ((size_t)b * p.Hq + hq) * p.T + i;
+        nl[e] = valid ? p.lse[row] * 1.4426950408889634f : INFINITY;
+        nd[e] = valid ? p.delta[row] : 0.f;
+      }
+    };
+    if (n > 0) fetch(0);
+    bool ok = true;
+    for (int u = 0; ok && u < n; ++u) {
+      const int q0 = (i_lo + u % n_tiles_per_head) * kBM;
       __syncwarp();
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int c = lane + 32 * e;
-        const int i = q0 + c;
-        const bool valid = i < p.T && i + off < L;
-        const size_t row = ((size_t)b * p.Hq + hq) * p.T + i;
-        st_lse[c] = valid ? p.lse[row] * 1.4426950408889634f : INFINITY;
-        st_dlt[c] = valid ? p.delta[row] : 0.f;
+        st_lse[lane + 32 * e] = nl[e];
+        st_dlt[lane + 32 * e] = nd[e];
       }
       __syncwarp();
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_mm, u & 1, 7, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
+      if (u + 1 < n) fetch(u + 1);
       // key kj is visible to query column c iff kj < L and (not causal or
       // kj <= q0 + c + off); invalid columns already have lse = +inf.
       const int c_min = p.causal ? kj - q0 - off : -1;  // visible columns: c >= c_min
-      const bool key_ok = kj < L;
+      const int c_min_warp = p.causal ? kj_warp_max - q0 - off : -1;
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        ok = __all_sync(0xffffffffu, mbar_wait(bar_mm0 + 8u * hh, u & 1, 7, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        const int cb = hh * kHalf;  // first query column of the half
+        // every (key, query) pair of the half visible for the whole warp
+        const int last = q0 + cb + kHalf - 1;
+        const bool dense = keys_ok && c_min_warp <= cb && last < p.T && last + off < L;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32], dp[32];
-        tmem_ld32(lane_base + kColS + 32 * c, sr);
-        tmem_ld32(lane_base + kColDP + 32 * c, dp);
-        tmem_wait_ld32(sr);
-        tmem_wait_ld32(dp);
-        uint32_t ppk[16], dpk[16];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sr[32], dp[32];
+          tmem_ld32(lane_base + col_s(hh) + 32 * c, sr);
+          tmem_ld32(lane_base + col_dp(hh) + 32 * c, dp);
+          tmem_wait_ld32(sr);
+          tmem_wait_ld32(dp);
+          uint32_t ppk[16], dpk[16];
+          const float* sl = st_lse + cb + 32 * c;
+          const float* sd = st_dlt + cb + 32 * c;
+          if (dense) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int col = 32 * c + e;
-          const float l0 = st_lse[col], l1 = st_lse[col + 1];
-          // selects, not products: hidden entries may hold NaN
-          const bool v0 = key_ok && col >= c_min && l0 != INFINITY;
-          const bool v1 = key_ok && col + 1 >= c_min && l1 != INFINITY;
-          const float e0 = ex2_approx(fmaf(__uint_as_float(sr[e]), sl2, -l0));
-          const float e1 = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), sl2, -l1));
-          const float p0 = v0 ? e0 : 0.f, p1 = v1 ? e1 : 0.f;
-          const float d0 = v0 ? e0 * (__uint_as_float(dp[e]) - st_dlt[col]) : 0.f;
-          const float d1 = v1 ? e1 * (__uint_as_float(dp[e + 1]) - st_dlt[col + 1]) : 0.f;
-          ppk[e >> 1] = pack2<kF16>(p0, p1);
-          dpk[e >> 1] = pack2<kF16>(d0, d1);
+            for (int e = 0; e < 32; e += 2) {
+              const float2 l = *reinterpret_cast<const float2*>(sl + e);
+              const float2 dl = *reinterpret_cast<const float2*>(sd + e);
+              const float2 x = __ffma2_rn(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                          sl2x2, make_float2(-l.x, -l.y));
+              const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              const float2 d = __fadd2_rn(make_float2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                          make_float2(-dl.x, -dl.y));
+              const float2 ds = __fmul2_rn(pe, d);
+              ppk[e >> 1] = pack2<kF16>(pe.x, pe.y);
+              dpk[e >> 1] = pack2<kF16>(ds.x, ds.y);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const int col = cb + 32 * c + e;
+              const float l0 = sl[e], l1 = sl[e + 1];
+              // selects, not products: hidden entries may hold NaN
+              const bool v0 = key_ok && col >= c_min && l0 != INFINITY;
+              const bool v1 = key_ok && col + 1 >= c_min && l1 != INFINITY;
+              const float e0 = ex2_approx(fmaf(__uint_as_float(sr[e]), sl2, -l0));
+              const float e1 = ex2_approx(fmaf(__uint_as_float(sr[e + 1]), sl2, -l1));
+              const float p0 = v0 ? e0 : 0.f, p1 = v1 ? e1 : 0.f;
+              const float d0 = v0 ? e0 * (__uint_as_float(dp[e]) - sd[e]) : 0.f;
+              const float d1 = v1 ? e1 * (__uint_as_float(dp[e + 1]) - sd[e + 1]) : 0.f;
+              ppk[e >> 1] = pack2<kF16>(p0, p1);
+              dpk[e >> 1] = pack2<kF16>(d0, d1);
+            }
+          }
+          tmem_st16(lane_base + col_s(hh) + 16 * c, ppk);
+          tmem_st16(lane_base + col_dp(hh) + 16 * c, dpk);
         }
-        tmem_st16(lane_base + kColS + 16 * c, ppk);
-        tmem_st16(lane_base + kColDP + 16 * c, dpk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(bar_pp0 + 8u * hh);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_p);
     }
     // ------------------------------------------------------------ epilogue
     if (ok && n > 0) ok = __all_sync(0xffffffffu, mbar_wait(bar_acc, 0, 8, abort_flag));

@@ -159,7 +159,7 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int T);
  * 0): their dQ is 0 and they add nothing to dK, dV.  Keys no row sees get
  * dK = dV = 0.  K/V rows at or past the valid length are never used.
  *
- *   q, o, dout  [B,Hq,T,D]   dtype (read)        dout must be finite
+ *   q, o, dout  [B,Hq,T,D]   dtype (read)        q, dout finite on every row
  *   k, v        [B,Hkv,S,D]  dtype (read)
  *   lse         [B,Hq,T]     float32 (read: attn_fwd's LSE for these inputs)
  *   dq          [B,Hq,T,D]   dtype (written)
@@ -171,7 +171,8 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int T);
  * Supported: ATTN_BF16 or ATTN_F16 with D in {64, 128} (tcgen05 tensor
  * cores, fp32 accumulation; P and dS are rounded to the input type for the
  * products); all
- * pointers 16-byte aligned (lse, key_lens, q_pos: 4).  ATTN_F32 returns
+ * pointers 16-byte aligned (lse, key_lens, q_pos: 4); B * Hq < 2^31 and at
+ * most 65535 tiles of 128 rows in T and in S.  ATTN_F32 returns
  * ATTN_ERR_UNSUPPORTED.  No atomics: results do not depend on scheduling.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
  * ATTN_ERR_WORKSPACE or ATTN_ERR_CUDA.
