@@ -175,6 +175,9 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* l
   if (items >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
   p.n_items = (int)items;
   p.o_align32 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
+  p.div_B = attn::make_fast_div((uint32_t)B);
+  p.div_Hq = attn::make_fast_div((uint32_t)Hq);
+  p.div_G = attn::make_fast_div((uint32_t)(Hq / Hkv));
   p.scale_log2 = scale * kLog2e;
   // Persistent: one CTA per SM (the kernel takes all 512 TMEM columns).
   const int grid = (int)std::min<long long>(num_sms(), items);

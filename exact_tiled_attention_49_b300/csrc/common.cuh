@@ -337,6 +337,26 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
 
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (TMA, tcgen05.mma operand reads).
+// Division of 0 <= n < 2^31 by an invariant d >= 1 with one multiply-high
+// and no divide sequence (whose reciprocal step would queue behind the
+// softmax's exponentials on the same pipe).  Granlund and Montgomery,
+// "Division by Invariant Integers using Multiplication" (PLDI 1994), the
+// round-up multiplier: with s = ceil(log2 d) and
+// m = floor(2^32 (2^s - d) / d) + 1, n / d = (umulhi(n, m) + n) >> s; the sum
+// stays below 2^32 because umulhi(n, m) < n < 2^31.
+struct FastDiv {
+  uint32_t m, s;
+};
+inline FastDiv make_fast_div(uint32_t d) {
+  uint32_t s = 0;
+  while ((1ull << s) < d) ++s;
+  const uint64_t m = ((1ull << 32) * ((1ull << s) - d)) / d + 1;
+  return FastDiv{(uint32_t)m, s};
+}
+__device__ __forceinline__ int fast_div(int n, FastDiv f) {
+  return (int)((__umulhi((uint32_t)n, f.m) + (uint32_t)n) >> f.s);
+}
+
 __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -71,8 +71,8 @@ struct Cfg {
   static constexpr int kNumBars = 2 + 2 + 2 * kSlots + 2 + 4 + 2 + 1 + 1;
   static constexpr uint32_t kOffMisc = kOffBars + 8 * kNumBars;    // TMEM address, abort flag
   static constexpr uint32_t kOffSched = (kOffMisc + 16 + 15) / 16 * 16;  // SchedArgs
-  static constexpr uint32_t kOffWalk = kOffSched + 48;                   // WalkState[warps][2]
-  static constexpr uint32_t kBytes = kOffWalk + 16 * 2 * (kThreads / 32);
+  static constexpr uint32_t kOffWalk = kOffSched + 64;                   // WalkState[warps][2]
+  static constexpr uint32_t kBytes = kOffWalk + 32 * 2 * (kThreads / 32);
   static constexpr size_t kSmemAlloc = kBytes + 1024;       // + alignment slack
   static constexpr uint32_t kColS(int t) { return (uint32_t)(t * kBN); }
   static constexpr uint32_t kColO(int t) { return (uint32_t)(2 * kBN + t * D); }
@@ -89,6 +89,7 @@ struct Params {
   int n_items;              // n_pairs * B * Hq
   int o_align32;            // o is 32-byte aligned: 256-bit stores
   float scale_log2;         // scale * log2(e)
+  FastDiv div_B, div_Hq, div_G;  // division by B, Hq and Hq / Hkv
 };
 
 struct Item {
@@ -130,12 +131,15 @@ struct SchedArgs {
   const int32_t* key_lens;
   const int32_t* q_pos;
   int n_pairs, B, Hq, T, S, causal, all_busy;
+  FastDiv div_B, div_Hq;
 };
 struct WalkState {
-  int g0;       // first group of the current 32-group window
-  int base;     // list index of the window's first item
-  int round;    // items handed out so far
-  int pad;
+  int g0;         // first group of the current 32-group window
+  int base;       // list index of the window's first item
+  int round;      // items handed out so far
+  int have;       // `mask` holds the current window's classification
+  uint32_t mask;  // groups of the window that are in the list (bit = lane)
+  int pad[3];
 };
 
 // Key tiles of the query tile starting at q0 (the rule of tile_count).
@@ -162,8 +166,12 @@ __device__ __forceinline__ int sched_tiles(const SchedArgs& a, int q0, int L, in
 // key padding and with T <= S (or no causal mask) no group is empty and the
 // item follows from its position in closed form; otherwise the warp
 // classifies 32 groups per step (ballot + prefix count), because a serial
-// walk costs about 200 cycles per group.  Every role of the CTA walks its
-// own copy and sees the same sequence.
+// walk costs about 200 cycles per group.  The classification of the current
+// window is kept in the walk state, and the divisions by B and Hq are
+// multiply-highs: a walk that reclassified its window and divided with the
+// divide sequence on every call took 2000-3700 cycles of the MMA warp at each
+// item boundary, mostly waiting behind the softmax warps' exponentials.
+// Every role of the CTA walks its own copy and sees the same sequence.
 template <bool kEmpty>
 __device__ __noinline__ uint64_t sched_next(const SchedArgs* args, WalkState* st) {
   const SchedArgs a = *args;
@@ -177,40 +185,49 @@ __device__ __noinline__ uint64_t sched_next(const SchedArgs* args, WalkState* st
   if (a.all_busy) {
     __syncwarp();
     if (kEmpty || target >= n_groups * a.Hq) return 0;
-    const int g = target / a.Hq;
-    const int pr = g / a.B;
+    const int g = fast_div(target, a.div_Hq);
+    const int pr = fast_div(g, a.div_B);
     return (1ull << 63) | ((uint64_t)(a.n_pairs - 1 - pr) << 32) |
            ((uint64_t)(g - pr * a.B) << 16) | (uint64_t)(target - g * a.Hq);
   }
-  int g0 = st->g0, base = st->base;
+  int g0 = st->g0, base = st->base, have = st->have;
+  uint32_t mask = st->mask;
   uint64_t res = 0;
-  for (; g0 < n_groups; g0 += 32) {
-    const int g = g0 + lane;
-    bool in_list = false;
-    if (g < n_groups) {
-      const int pr = g / a.B, b = g - pr * a.B;
-      const int q0 = (a.n_pairs - 1 - pr) * kItemRows;
-      const int L = a.key_lens != nullptr ? min(max(a.key_lens[b], 0), a.S) : a.S;
-      const int off = q_offset(a.q_pos, b, a.T, a.S);
-      const bool busy = sched_tiles(a, q0, L, off) > 0 || sched_tiles(a, q0 + kBM, L, off) > 0;
-      in_list = busy != kEmpty;
+  while (g0 < n_groups) {
+    if (!have) {
+      const int g = g0 + lane;
+      bool in_list = false;
+      if (g < n_groups) {
+        const int pr = fast_div(g, a.div_B), b = g - pr * a.B;
+        const int q0 = (a.n_pairs - 1 - pr) * kItemRows;
+        const int L = a.key_lens != nullptr ? min(max(a.key_lens[b], 0), a.S) : a.S;
+        const int off = q_offset(a.q_pos, b, a.T, a.S);
+        const bool busy = sched_tiles(a, q0, L, off) > 0 || sched_tiles(a, q0 + kBM, L, off) > 0;
+        in_list = busy != kEmpty;
+      }
+      mask = __ballot_sync(0xffffffffu, in_list);
+      have = 1;
     }
-    const uint32_t mask = __ballot_sync(0xffffffffu, in_list);
     const int cnt = __popc(mask) * a.Hq;
     if (target < base + cnt) {
-      const int k = (target - base) / a.Hq;
-      const bool mine = in_list && __popc(mask & ((1u << lane) - 1u)) == k;
+      // the k-th set bit of the mask is the group that holds the target
+      const int k = fast_div(target - base, a.div_Hq);
+      const bool mine = ((mask >> lane) & 1u) && __popc(mask & ((1u << lane) - 1u)) == k;
       const int gs = g0 + __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
-      const int pr = gs / a.B;
+      const int pr = fast_div(gs, a.div_B);
       res = (1ull << 63) | ((uint64_t)(a.n_pairs - 1 - pr) << 32) |
             ((uint64_t)(gs - pr * a.B) << 16) | (uint64_t)(target - base - k * a.Hq);
       break;  // later targets are larger: keep this window
     }
     base += cnt;
+    g0 += 32;
+    have = 0;
   }
   if (lane == 0) {
     st->g0 = g0;
     st->base = base;
+    st->have = have;
+    st->mask = mask;
   }
   __syncwarp();
   return res;
@@ -300,10 +317,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     sched->T = p.T;
     sched->S = p.S;
     sched->causal = p.causal;
+    sched->div_B = p.div_B;
+    sched->div_Hq = p.div_Hq;
     sched->all_busy =
         p.key_lens == nullptr && p.q_pos == nullptr && (!p.causal || p.T <= p.S);
   }
-  if (lane == 0) walk[0] = walk[1] = WalkState{0, 0, 0, 0};
+  if (lane == 0) walk[0] = walk[1] = WalkState{0, 0, 0, 0, 0u, {0, 0, 0}};
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
@@ -335,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nm = max(n0, n1);
       if (nm == 0) continue;
       const int bh_q = it.b * p.Hq + it.h;
-      const int bh_kv = it.b * p.Hkv + it.h / (p.Hq / p.Hkv);
+      const int bh_kv = it.b * p.Hkv + fast_div(it.h, p.div_G);
       // The V tile that holds key rows at or past L, if L falls inside a
       // tile below S: those rows get P = 0, but 0 * NaN is NaN, so they are
       // zeroed before P V can read them (a cache's unused tail may hold

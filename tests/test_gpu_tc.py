@@ -57,6 +57,9 @@ CASES = [
     (2, 8, 2, 513, 513, 128, True, (200, 513)),
     (1, 2, 2, 77, 1000, 64, False, None),
     (3, 4, 4, 640, 640, 128, True, (0, 640)),
+    # odd B, Hq and group size: the work walk divides by B, Hq and Hq / Hkv
+    (3, 6, 2, 700, 700, 64, True, (100, 700)),
+    (5, 3, 3, 300, 300, 128, True, None),
 ]
 
 
