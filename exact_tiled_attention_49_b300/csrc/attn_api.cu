@@ -170,7 +170,13 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* l
   p.T = T;
   p.S = S;
   p.causal = causal ? 1 : 0;
-  p.n_pairs = (T + kItemRows - 1) / kItemRows;
+  // Pair slots per (batch, head): a sequence whose count of query tiles
+  // with a non-padded row is odd has its pairs shifted 128 rows down, so it
+  // needs room for T + 128 rows.  Without key_lens and q_pos every sequence
+  // has ceil(T / 128) such tiles.
+  const int shift_all = (((T + kBM - 1) / kBM) & 1) ? kBM : 0;
+  const int span = (key_lens != nullptr || q_pos != nullptr) ? T + kBM : T + shift_all;
+  p.n_pairs = (span + kItemRows - 1) / kItemRows;
   const long long items = (long long)p.n_pairs * B * Hq;
   if (items >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
   p.n_items = (int)items;

@@ -85,7 +85,8 @@ struct Params {
   const int32_t* q_pos;     // [B] key position of query row 0, or null (S - T)
   int B, Hq, Hkv, T, S;
   int causal;
-  int n_pairs;              // ceil(T / 256)
+  int n_pairs;              // pair slots per (batch, head): enough for T + 128 rows
+                            // when a sequence's pairs may be shifted
   int n_items;              // n_pairs * B * Hq
   int o_align32;            // o is 32-byte aligned: 256-bit stores
   float scale_log2;         // scale * log2(e)
@@ -109,12 +110,25 @@ __device__ __forceinline__ int q_offset(const int32_t* q_pos, int b, int T, int 
   return q_pos != nullptr ? min(max(q_pos[b], -(T + 256)), S) : S - T;
 }
 
+// Pairing of query tiles.  The query tiles of a sequence that hold at least
+// one non-padded row are paired from the top: when their count is odd, every
+// pair of the sequence starts 128 rows lower (the shift), so the tile left
+// without a partner is tile 0, which visits the fewest key tiles under a
+// causal mask, instead of the last and heaviest one.  A shifted sequence's
+// first pair then has a virtual tile at rows -128..-1, which has no rows, no
+// key tiles and no loads.
+__device__ __forceinline__ int seq_shift(int T, int L, int off) {
+  const int rows = min(T, L - off);  // rows below this are not padded
+  const int tiles = rows > 0 ? (rows + kBM - 1) / kBM : 0;
+  return (tiles & 1) ? kBM : 0;
+}
+
 // Number of key tiles the query tile starting at row q0 must visit (0 when
-// every row of the tile is past T, padded, or sees no key); `off` is the
-// sequence's q_offset.  Every role computes it the same way so they agree
-// on the trip counts.
+// every row of the tile is past T, padded, virtual or sees no key); `off` is
+// the sequence's q_offset.  Every role computes it the same way so they
+// agree on the trip counts.
 __device__ __forceinline__ int tile_count(const Params& p, int q0, int L, int off) {
-  if (q0 >= p.T) return 0;
+  if (q0 < 0 || q0 >= p.T) return 0;
   if (q0 + off >= L) return 0;  // every row of the tile is a padded row
   int kv_end = L;
   if (p.causal) kv_end = min(L, q0 + kBM + off);  // last row sees keys <= q0+BM-1+off
@@ -132,25 +146,28 @@ struct SchedArgs {
   const int32_t* q_pos;
   int n_pairs, B, Hq, T, S, causal, all_busy;
   FastDiv div_B, div_Hq;
+  int shift_all;  // the shift of every sequence (closed-form walk)
 };
+static_assert(sizeof(SchedArgs) <= 64, "SchedArgs fits its shared-memory slot");
 struct WalkState {
   int g0;         // first group of the current 32-group window
   int base;       // list index of the window's first item
   int round;      // items handed out so far
   int have;       // `mask` holds the current window's classification
   uint32_t mask;  // groups of the window that are in the list (bit = lane)
-  int pad[3];
+  uint32_t smask; // groups of the window whose sequence is shifted
+  int pad[2];
 };
 
 // Key tiles of the query tile starting at q0 (the rule of tile_count).
 __device__ __forceinline__ int sched_tiles(const SchedArgs& a, int q0, int L, int off) {
-  if (q0 >= a.T || q0 + off >= L) return 0;
+  if (q0 < 0 || q0 >= a.T || q0 + off >= L) return 0;
   const int kv_end = a.causal ? min(L, q0 + kBM + off) : L;
   return kv_end <= 0 ? 0 : (kv_end + kBN - 1) / kBN;
 }
 
-// Next work item of this CTA, packed as valid << 63 | pair << 32 | b << 16 | h
-// (0 when there is none).
+// Next work item of this CTA, packed as valid << 63 | shifted << 62 |
+// pair << 32 | b << 16 | h (0 when there is none).
 //
 // The items are ordered pair-descending (the heaviest causal work first),
 // then by batch and head; a "group" is the Hq items of one (pair, batch).
@@ -187,25 +204,29 @@ __device__ __noinline__ uint64_t sched_next(const SchedArgs* args, WalkState* st
     if (kEmpty || target >= n_groups * a.Hq) return 0;
     const int g = fast_div(target, a.div_Hq);
     const int pr = fast_div(g, a.div_B);
-    return (1ull << 63) | ((uint64_t)(a.n_pairs - 1 - pr) << 32) |
-           ((uint64_t)(g - pr * a.B) << 16) | (uint64_t)(target - g * a.Hq);
+    return (1ull << 63) | ((uint64_t)(a.shift_all != 0) << 62) |
+           ((uint64_t)(a.n_pairs - 1 - pr) << 32) | ((uint64_t)(g - pr * a.B) << 16) |
+           (uint64_t)(target - g * a.Hq);
   }
   int g0 = st->g0, base = st->base, have = st->have;
-  uint32_t mask = st->mask;
+  uint32_t mask = st->mask, smask = st->smask;
   uint64_t res = 0;
   while (g0 < n_groups) {
     if (!have) {
       const int g = g0 + lane;
-      bool in_list = false;
+      bool in_list = false, shifted = false;
       if (g < n_groups) {
         const int pr = fast_div(g, a.div_B), b = g - pr * a.B;
-        const int q0 = (a.n_pairs - 1 - pr) * kItemRows;
         const int L = a.key_lens != nullptr ? min(max(a.key_lens[b], 0), a.S) : a.S;
         const int off = q_offset(a.q_pos, b, a.T, a.S);
+        const int sh = seq_shift(a.T, L, off);
+        const int q0 = (a.n_pairs - 1 - pr) * kItemRows - sh;
         const bool busy = sched_tiles(a, q0, L, off) > 0 || sched_tiles(a, q0 + kBM, L, off) > 0;
         in_list = busy != kEmpty;
+        shifted = sh != 0;
       }
       mask = __ballot_sync(0xffffffffu, in_list);
+      smask = __ballot_sync(0xffffffffu, shifted);
       have = 1;
     }
     const int cnt = __popc(mask) * a.Hq;
@@ -213,10 +234,12 @@ __device__ __noinline__ uint64_t sched_next(const SchedArgs* args, WalkState* st
       // the k-th set bit of the mask is the group that holds the target
       const int k = fast_div(target - base, a.div_Hq);
       const bool mine = ((mask >> lane) & 1u) && __popc(mask & ((1u << lane) - 1u)) == k;
-      const int gs = g0 + __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+      const int ls = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+      const int gs = g0 + ls;
       const int pr = fast_div(gs, a.div_B);
-      res = (1ull << 63) | ((uint64_t)(a.n_pairs - 1 - pr) << 32) |
-            ((uint64_t)(gs - pr * a.B) << 16) | (uint64_t)(target - base - k * a.Hq);
+      res = (1ull << 63) | ((uint64_t)((smask >> ls) & 1u) << 62) |
+            ((uint64_t)(a.n_pairs - 1 - pr) << 32) | ((uint64_t)(gs - pr * a.B) << 16) |
+            (uint64_t)(target - base - k * a.Hq);
       break;  // later targets are larger: keep this window
     }
     base += cnt;
@@ -228,6 +251,7 @@ __device__ __noinline__ uint64_t sched_next(const SchedArgs* args, WalkState* st
     st->base = base;
     st->have = have;
     st->mask = mask;
+    st->smask = smask;
   }
   __syncwarp();
   return res;
@@ -236,7 +260,7 @@ __device__ __noinline__ uint64_t sched_next(const SchedArgs* args, WalkState* st
 // Unpacks a sched_next result; false when the walk is over.
 __device__ __forceinline__ bool unpack_item(uint64_t v, Item& it) {
   if (!(v >> 63)) return false;
-  it.q0 = (int)((v >> 32) & 0x7FFFFFFFu) * kItemRows;
+  it.q0 = (int)((v >> 32) & 0x3FFFFFFFu) * kItemRows - (int)((v >> 62) & 1u) * kBM;
   it.b = (int)((v >> 16) & 0xFFFFu);
   it.h = (int)(v & 0xFFFFu);
   return true;
@@ -319,10 +343,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     sched->causal = p.causal;
     sched->div_B = p.div_B;
     sched->div_Hq = p.div_Hq;
+    sched->shift_all = seq_shift(p.T, p.S, p.S - p.T);
     sched->all_busy =
         p.key_lens == nullptr && p.q_pos == nullptr && (!p.causal || p.T <= p.S);
   }
-  if (lane == 0) walk[0] = walk[1] = WalkState{0, 0, 0, 0, 0u, {0, 0, 0}};
+  if (lane == 0) walk[0] = walk[1] = WalkState{0, 0, 0, 0, 0u, 0u, {0, 0}};
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_holder), kTmemCols);
     tmem_relinquish();
@@ -346,56 +371,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool w = mbar_wait(bar, parity, 1, abort_flag);
       return __all_sync(0xffffffffu, w);
     };
-        Item it;
-    while (ok && unpack_item(sched_next<false>(sched, walk), it)) {
-      const int L = key_bound(p, it.b);
-      const int off = q_offset(p.q_pos, it.b, p.T, p.S);
-      const int n0 = tile_count(p, it.q0, L, off), n1 = tile_count(p, it.q0 + kBM, L, off);
-      const int nm = max(n0, n1);
-      if (nm == 0) continue;
-      const int bh_q = it.b * p.Hq + it.h;
-      const int bh_kv = it.b * p.Hkv + fast_div(it.h, p.div_G);
-      // The V tile that holds key rows at or past L, if L falls inside a
-      // tile below S: those rows get P = 0, but 0 * NaN is NaN, so they are
-      // zeroed before P V can read them (a cache's unused tail may hold
-      // anything; rows past S are zero-filled by TMA already).  That tile
-      // lands on a private barrier; this warp zeroes the rows and then
-      // completes the slot's full barrier itself.
-      const int j_tail = (L < p.S && (L & (kBN - 1)) != 0) ? L / kBN : -1;
-      for (int t = 0; t < kQTiles && ok; ++t) {
-        if (qi > 0) ok = wait_bar(bar_qempty(t), (qi - 1) & 1);
-        if (!ok) break;
-        if (lane == 0) {
+    // Next item with key tiles to visit (false when the walk is over).
+    auto next_item = [&](Item& x, int& L, int& off, int& n0, int& n1) {
+      while (unpack_item(sched_next<false>(sched, walk), x)) {
+        L = key_bound(p, x.b);
+        off = q_offset(p.q_pos, x.b, p.T, p.S);
+        n0 = tile_count(p, x.q0, L, off);
+        n1 = tile_count(p, x.q0 + kBM, L, off);
+        if (max(n0, n1) > 0) return true;
+      }
+      return false;
+    };
+    // Query tile t of the item with row x.q0 into its buffer (qi-th use).
+    auto load_q = [&](const Item& x, int t) {
+      if (qi > 0 && !(ok = wait_bar(bar_qempty(t), (qi - 1) & 1))) return;
+      if (lane == 0) {
+        if (x.q0 + t * kBM < 0) {
+          mbar_arrive(bar_qfull(t));  // virtual tile: nothing to load
+        } else {
           mbar_arrive_expect_tx(bar_qfull(t), C::kQBytes);
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(s_q + t * C::kQBytes + c * C::kChunkBytes, &tm_q, bar_qfull(t), c * 64,
-                        it.q0 + t * kBM, bh_q);
+                        x.q0 + t * kBM, x.b * p.Hq + x.h);
         }
       }
+    };
+    // One K or V tile into the next ring slot.  `zero_from` >= 0: a V tile
+    // that holds key rows at or past the valid length L (those rows get
+    // P = 0, but 0 * NaN is NaN, so they are zeroed before P V can read them;
+    // a cache's unused tail may hold anything, rows past S are zero-filled
+    // by TMA already).  That tile lands on a private barrier; this warp
+    // zeroes the rows and then completes the slot's full barrier itself.
+    auto load_kv = [&](const CUtensorMap* tm, int row, int bh_kv, int zero_from) {
+      const int slot = ring % C::kSlots;
+      if (ring >= C::kSlots && !(ok = wait_bar(bar_empty(slot), ((ring / C::kSlots) - 1) & 1)))
+        return;
+      const uint32_t dst = s_slots + slot * C::kTileBytes;
+      const bool tail = zero_from >= 0;
+      const uint32_t bar_land = tail ? bar_tail : bar_full(slot);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(bar_land, C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          tma_load_3d(dst + c * C::kChunkBytes, tm, bar_land, c * 64, row, bh_kv);
+      }
+      if (tail) {
+        ok = wait_bar(bar_tail, ntail & 1);
+        ++ntail;
+        if (!ok) return;
+        zero_rows_from<C::kChunks>(dst, zero_from, lane);
+        if (lane == 0) mbar_arrive(bar_full(slot));
+      }
+      ++ring;
+    };
+    Item it, nx;
+    int L = 0, off = 0, n0 = 0, n1 = 0;
+    bool have = next_item(it, L, off, n0, n1);
+    bool early = false;  // Q_0 and K_0 of `it` went out with the previous item
+    while (ok && have) {
+      const int nm = max(n0, n1);
+      const int bh_kv = it.b * p.Hkv + fast_div(it.h, p.div_G);
+      const int j_tail = (L < p.S && (L & (kBN - 1)) != 0) ? L / kBN : -1;
+      if (!early) load_q(it, 0);
+      if (ok) load_q(it, 1);
+      if (!ok) break;
       ++qi;
+      int nL = 0, noff = 0, nn0 = 0, nn1 = 0;
+      const bool have_nx = next_item(nx, nL, noff, nn0, nn1);
+      // With a causal diagonal (tile 1 visits one key tile more than tile 0)
+      // the MMA warp starts the next item's tile 0 while tile 1 finishes
+      // alone: that item's Q_0 and K_0 go out between this item's last K and
+      // last V, the order the MMA warp consumes them.
+      const bool early_next = have_nx && n0 >= 1 && n1 == n0 + 1;
       // K_0, V_0, K_1, V_1, ...: the order the MMA warp consumes them.
-      for (int u = 0; ok && u < 2 * nm; ++u) {
-        const int slot = ring % C::kSlots;
-        if (ring >= C::kSlots) ok = wait_bar(bar_empty(slot), ((ring / C::kSlots) - 1) & 1);
-        if (!ok) break;
-        const uint32_t dst = s_slots + slot * C::kTileBytes;
-        const bool tail = (u & 1) && (u >> 1) == j_tail;
-        const uint32_t bar_land = tail ? bar_tail : bar_full(slot);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar_land, C::kTileBytes);
-          const CUtensorMap* tm = (u & 1) ? &tm_v : &tm_k;
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(dst + c * C::kChunkBytes, tm, bar_land, c * 64, (u >> 1) * kBN, bh_kv);
-        }
-        if (tail) {
-          ok = wait_bar(bar_tail, ntail & 1);
-          ++ntail;
+      for (int u = early ? 1 : 0; ok && u < 2 * nm; ++u) {
+        if (u == 2 * nm - 1 && early_next) {
+          load_q(nx, 0);
+          if (ok) load_kv(&tm_k, 0, nx.b * p.Hkv + fast_div(nx.h, p.div_G), -1);
           if (!ok) break;
-          zero_rows_from<C::kChunks>(dst, L & (kBN - 1), lane);
-          if (lane == 0) mbar_arrive(bar_full(slot));
         }
-        ++ring;
+        const bool is_v = u & 1;
+        const int zero_from = (is_v && (u >> 1) == j_tail) ? (L & (kBN - 1)) : -1;
+        load_kv(is_v ? &tm_v : &tm_k, (u >> 1) * kBN, bh_kv, zero_from);
       }
+      it = nx;
+      L = nL;
+      off = noff;
+      n0 = nn0;
+      n1 = nn1;
+      have = have_nx;
+      early = early_next;
     }
     // Drain: every issued copy must land before the CTA may exit (the last
     // kSlots ring entries cover every slot's latest copy).
@@ -449,35 +513,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                       idesc_pv, (acc || kk > 0) ? 1u : 0u);
       }
     };
-        Item it;
-    while (ok && unpack_item(sched_next<false>(sched, walk), it)) {
-      const int L = key_bound(p, it.b);
-      const int off = q_offset(p.q_pos, it.b, p.T, p.S);
-      const int n0 = tile_count(p, it.q0, L, off), n1 = tile_count(p, it.q0 + kBM, L, off);
-      const int nm = max(n0, n1);
-      if (nm == 0) continue;
-      ok = wait_bar(bar_qfull(0), qi & 1) && wait_bar(bar_qfull(1), qi & 1);
-      ++qi;
-      if (!ok) break;
-      // K_0: the first score tile of both query tiles.
-      int kslot = ring % C::kSlots;
-      if (!(ok = wait_slot(ring))) break;
-      ++ring;
-      tc_fence_after();
-#pragma unroll
-      for (int t = 0; t < kQTiles; ++t) {
-        const int nt = t ? n1 : n0;
-        if (nt > 0) issue_qk(t, kslot);
-        if (nt <= 1) umma_commit_elect(bar_qempty(t));  // Q_t read for the last time
+    // Next item with key tiles to visit and its tile counts (false when the
+    // walk is over); the same sequence the load warp walks.
+    auto next_item = [&](int& n0, int& n1) {
+      Item x;
+      while (unpack_item(sched_next<false>(sched, walk), x)) {
+        const int L = key_bound(p, x.b);
+        const int off = q_offset(p.q_pos, x.b, p.T, p.S);
+        n0 = tile_count(p, x.q0, L, off);
+        n1 = tile_count(p, x.q0 + kBM, L, off);
+        if (max(n0, n1) > 0) return true;
       }
-      umma_commit_elect(bar_empty(kslot));
+      return false;
+    };
+    // S_t(0) of an item from its K_0 in `slot`; Q_t is read for the last time
+    // when the tile visits at most one key tile.
+    auto first_qk = [&](int t, int nt, int slot) {
+      if (nt > 0) issue_qk(t, slot);
+      if (nt <= 1) umma_commit_elect(bar_qempty(t));
+    };
+    int n0 = 0, n1 = 0;
+    bool have = next_item(n0, n1);
+    bool early = false;  // S_0(0) of the current item went out with the previous item
+    int kslot0 = 0;      // ring slot of the current item's K_0
+    while (ok && have) {
+      const int nm = max(n0, n1);
+      if (!early) {
+        if (!(ok = wait_bar(bar_qfull(0), qi & 1))) break;
+        kslot0 = ring % C::kSlots;
+        if (!(ok = wait_slot(ring))) break;
+        ++ring;
+        tc_fence_after();
+        first_qk(0, n0, kslot0);
+      }
+      if (!(ok = wait_bar(bar_qfull(1), qi & 1))) break;
+      ++qi;
+      tc_fence_after();
+      first_qk(1, n1, kslot0);
+      umma_commit_elect(bar_empty(kslot0));
+      int nn0 = 0, nn1 = 0;
+      const bool have_nx = next_item(nn0, nn1);
+      // Causal diagonal: tile 1 visits one key tile more than tile 0.  Once
+      // tile 0 is done (step n0 - 1) the next item's S_0(0) is issued from its
+      // K_0, which the load warp placed between this item's last K and V, so
+      // the tensor core is busy while tile 1 finishes alone.
+      const bool early_next = have_nx && n0 >= 1 && n1 == n0 + 1;
+      early = false;
       for (int j = 0; ok && j < nm; ++j) {
         const int vslot = ring % C::kSlots;
         if (!(ok = wait_slot(ring))) break;
         ++ring;
         const bool has_next = j + 1 < nm;
         bool next_ready = false;
-        kslot = ring % C::kSlots;
+        const int kslot = ring % C::kSlots;
         tc_fence_after();
 #pragma unroll
         for (int t = 0; t < kQTiles; ++t) {
@@ -512,7 +600,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit_elect(bar_empty(kslot));
           ++ring;
         }
+        if (early_next && j == n0 - 1) {
+          // Q_0 and K_0 of the next item (qi already counts this item)
+          if (!(ok = wait_bar(bar_qfull(0), qi & 1))) break;
+          kslot0 = ring % C::kSlots;
+          if (!(ok = wait_slot(ring))) break;
+          ++ring;
+          tc_fence_after();
+          first_qk(0, nn0, kslot0);
+          early = true;
+        }
       }
+      n0 = nn0;
+      n1 = nn1;
+      have = have_nx;
     }
     // Drain: all issued MMAs complete before TMEM is released.
     umma_commit_elect(bar_drain);
@@ -538,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = tile_count(p, q0t, L, off);
       const int i = q0t + r;
       const int pos = i + off;
-      const bool row_ok = (i < p.T) && (pos < L);
+      const bool row_ok = (i >= 0) && (i < p.T) && (pos < L);
       const int lim = p.causal ? min(L, pos + 1) : L;  // visible keys: [0, lim)
       float m_ref = -INFINITY;  // exponent reference (log2 units)
       float l = 0.f;
@@ -668,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e)
             pkd[e] = pack2<kF16>(__uint_as_float(orr[2 * e]) * inv,
                                  __uint_as_float(orr[2 * e + 1]) * inv);
-          if (i < p.T) {
+          if (i >= 0 && i < p.T) {
             uint16_t* dst = orow + 64 * c;
             if (p.o_align32) {
 #pragma unroll
@@ -682,11 +783,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-      } else if (i < p.T) {
+      } else if (i >= 0 && i < p.T) {
         uint4* dst = reinterpret_cast<uint4*>(orow);
         for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0, 0, 0, 0);
       }
-      if (p.lse != nullptr && i < p.T) {
+      if (p.lse != nullptr && i >= 0 && i < p.T) {
         p.lse[((size_t)it.b * p.Hq + it.h) * p.T + i] =
             has ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
@@ -694,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Items with no key tile: every row is padded (or past T): O = 0, LSE = -inf.
     while (ok && unpack_item(sched_next<true>(sched, walk + 1), it)) {
       const int i = it.q0 + t * kBM + r;
-      if (i >= p.T) continue;
+      if (i < 0 || i >= p.T) continue;
       const size_t row = ((size_t)it.b * p.Hq + it.h) * p.T + i;
       uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.o) + row * D);
 #pragma unroll
