@@ -32,6 +32,38 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return u32.view(np.float32).astype(np.float64)
 
 
+def e4m3_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of FP8 E4M3 bit patterns (uint8) to float64.
+
+    The format of the FP8 inputs that "Self-Attention: Implementation,
+    Complexity, and Efficient Variants" (FlashAttention-3: FP8 support)
+    refers to, as published in "FP8 Formats for Deep Learning" (Micikevicius
+    et al., 2022) and the OCP 8-bit floating point specification: one sign
+    bit, four exponent bits with bias 7, three mantissa bits; exponent field 0
+    holds the subnormals m/8 * 2^-6; there are no infinities and S.1111.111 is
+    NaN, so the largest finite magnitude is 1.75 * 2^8 = 448.
+    """
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0))
+    val = np.where((e == 0xF) & ((b & 0x7) == 0x7), np.nan, val)
+    return sign * val
+
+
+def attn_fwd_fp8_np(q8, k8, v8, q_descale=1.0, k_descale=1.0, v_descale=1.0, causal=False,
+                    key_lens=None, scale=None):
+    """Attention on FP8 E4M3 inputs: the plain definition of attn_fwd_np
+    applied to the dequantised inputs q = q8 * q_descale, k = k8 * k_descale,
+    v = v8 * v_descale (per-tensor scales, the FlashAttention-3 convention),
+    in float64.  Returns (o, lse)."""
+    q = e4m3_bits_to_f64(q8) * q_descale
+    k = e4m3_bits_to_f64(k8) * k_descale
+    v = e4m3_bits_to_f64(v8) * v_descale
+    return attn_fwd_np(q, k, v, causal=causal, key_lens=key_lens, scale=scale)
+
+
 def _as_f64(x: np.ndarray, bf16: bool) -> np.ndarray:
     if bf16:
         return bf16_bits_to_f64(np.asarray(x, dtype=np.uint16))
