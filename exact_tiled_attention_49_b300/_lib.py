@@ -25,6 +25,8 @@ SIGNATURES = {
     "attn_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _F, _P]),
     "attn_fwd_chunked": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F,
                               _P]),
+    "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _F, _F, _F, _F,
+                          _P]),
     "attn_bwd_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P,
                       _F, _P, ctypes.c_size_t, _P]),
@@ -146,6 +148,46 @@ def attn_fwd(q, k, v, o=None, lse=None, causal=False, key_lens=None, scale=None,
     rc = lib.attn_fwd(*ptrs, lp, B, Hq, Hkv, T, S, D, dt, int(bool(causal)), kl,
                       float(scale), _stream(stream))
     _check(rc, "attn_fwd")
+    return o, lse
+
+
+def attn_fwd_fp8(q, k, v, o=None, lse=None, causal=False, key_lens=None, scale=None,
+                 q_descale=1.0, k_descale=1.0, v_descale=1.0, return_lse=True, stream=None):
+    """Prefill forward on FP8 E4M3 inputs: attention of q_descale*q,
+    k_descale*k, v_descale*v.  q [B,Hq,T,128], k/v [B,Hkv,S,128] as
+    torch.float8_e4m3fn (or their uint8 bytes), CUDA.  Returns (o, lse) with
+    o bfloat16 [B,Hq,T,128] and lse float32 [B,Hq,T]."""
+    lib = load()
+    B, Hq, T, D = q.shape
+    Bk, Hkv, S, Dk = k.shape
+    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q/k/v shape mismatch")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype not in (torch.float8_e4m3fn, torch.uint8):
+            raise TypeError(f"{name} must be float8_e4m3fn (or its uint8 bytes)")
+    if o is None:
+        o = torch.empty(q.shape, device=q.device, dtype=torch.bfloat16)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, T), device=q.device, dtype=torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    ptrs = [_dev(q, "q", ndim=4), _dev(k, "k", ndim=4), _dev(v, "v", ndim=4),
+            _dev(o, "o", dtype=torch.bfloat16, ndim=4)]
+    if tuple(o.shape) != tuple(q.shape):
+        raise ValueError("o must have q's shape")
+    lp = None
+    if lse is not None:
+        lp = _dev(lse, "lse", dtype=torch.float32)
+        if lse.numel() != B * Hq * T:
+            raise ValueError("lse must hold B*Hq*T floats")
+    kl = None
+    if key_lens is not None:
+        kl = _dev(key_lens, "key_lens", dtype=torch.int32, ndim=1)
+        if key_lens.numel() != B:
+            raise ValueError("key_lens must have B entries")
+    rc = lib.attn_fwd_fp8(*ptrs, lp, B, Hq, Hkv, T, S, D, int(bool(causal)), kl, float(scale),
+                          float(q_descale), float(k_descale), float(v_descale), _stream(stream))
+    _check(rc, "attn_fwd_fp8")
     return o, lse
 
 

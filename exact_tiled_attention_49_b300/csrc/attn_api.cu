@@ -71,6 +71,21 @@ bool make_tmap_bf16(CUtensorMap* m, const void* base, int D, int rows, long long
   return r == CUDA_SUCCESS;
 }
 
+// 3-D 8-bit tensor [outer, rows, D] (D = 128 contiguous, E4M3 bytes) loaded
+// as boxes of 128 columns x 128 rows with 128-byte swizzle.
+bool make_tmap_u8(CUtensorMap* m, const void* base, int D, int rows, long long outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)rows, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)rows * (cuuint64_t)D};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2-D 16-bit tensor [rows, D] (D contiguous; bf16, or fp16 when f16) loaded
 // as boxes of 64 columns x `box_rows` rows with 128-byte swizzle.
 bool make_tmap_bf16_2d(CUtensorMap* m, const void* base, int D, long long rows, int box_rows,
@@ -146,19 +161,29 @@ int launch_status() {
 
 // ------------------------------------------------------------- prefill
 
-template <int D, bool kF16>
+// kF8: E4M3 inputs with per-tensor descales (qkv_descale), bf16 output.
+template <int D, bool kF16, bool kF8 = false>
 int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                   int Hq, int Hkv, int T, int S, int causal, const int32_t* key_lens,
-                  const int32_t* q_pos, float scale, cudaStream_t st) {
+                  const int32_t* q_pos, float scale, cudaStream_t st,
+                  const float* qkv_descale = nullptr) {
   using namespace attn::tcfwd;
+  using C = Cfg<D, kF8 ? 1 : 2>;
   static std::atomic<uint64_t> smem_done{0};
-  auto kernel = fwd_bf16_tc_kernel<D, kF16>;
-  if (!ensure_smem(kernel, Cfg<D>::kSmemAlloc, smem_done)) return ATTN_ERR_CUDA;
+  auto kernel = fwd_bf16_tc_kernel<D, kF16, kF8>;
+  if (!ensure_smem(kernel, C::kSmemAlloc, smem_done)) return ATTN_ERR_CUDA;
   CUtensorMap tq, tk, tv;
-  if (!make_tmap_bf16(&tq, q, D, T, (long long)B * Hq, kF16) ||
-      !make_tmap_bf16(&tk, k, D, S, (long long)B * Hkv, kF16) ||
-      !make_tmap_bf16(&tv, v, D, S, (long long)B * Hkv, kF16))
-    return ATTN_ERR_CUDA;
+  if constexpr (kF8) {
+    if (!make_tmap_u8(&tq, q, D, T, (long long)B * Hq) ||
+        !make_tmap_u8(&tk, k, D, S, (long long)B * Hkv) ||
+        !make_tmap_u8(&tv, v, D, S, (long long)B * Hkv))
+      return ATTN_ERR_CUDA;
+  } else {
+    if (!make_tmap_bf16(&tq, q, D, T, (long long)B * Hq, kF16) ||
+        !make_tmap_bf16(&tk, k, D, S, (long long)B * Hkv, kF16) ||
+        !make_tmap_bf16(&tv, v, D, S, (long long)B * Hkv, kF16))
+      return ATTN_ERR_CUDA;
+  }
   Params p;
   p.o = o;
   p.lse = lse;
@@ -185,9 +210,14 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* l
   p.div_Hq = attn::make_fast_div((uint32_t)Hq);
   p.div_G = attn::make_fast_div((uint32_t)(Hq / Hkv));
   p.scale_log2 = scale * kLog2e;
+  p.o_scale = 1.f;
+  if constexpr (kF8) {
+    p.scale_log2 = scale * qkv_descale[0] * qkv_descale[1] * kLog2e;
+    p.o_scale = qkv_descale[2];
+  }
   // Persistent: one CTA per SM (the kernel takes all 512 TMEM columns).
   const int grid = (int)std::min<long long>(num_sms(), items);
-  kernel<<<grid, kThreads, Cfg<D>::kSmemAlloc, st>>>(tq, tk, tv, p);
+  kernel<<<grid, kThreads, C::kSmemAlloc, st>>>(tq, tk, tv, p);
   return launch_status();
 }
 
@@ -359,6 +389,24 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              float scale, attn_stream_t stream) {
   return fwd_dispatch(q, k, v, o, lse, B, Hq, Hkv, T, S, D, dtype, causal, key_lens, nullptr,
                       scale, stream);
+}
+
+int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                 int Hkv, int T, int S, int D, int causal, const int32_t* key_lens, float scale,
+                 float q_descale, float k_descale, float v_descale, attn_stream_t stream) {
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || S <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !finite_positive(scale) || !finite_positive(q_descale) ||
+      !finite_positive(k_descale) || !finite_positive(v_descale))
+    return ATTN_ERR_INVALID_ARG;
+  if (D != 128 || B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return ATTN_ERR_INVALID_ARG;
+  if (lse != nullptr && !aligned4(lse)) return ATTN_ERR_INVALID_ARG;
+  if (key_lens != nullptr && !aligned4(key_lens)) return ATTN_ERR_INVALID_ARG;
+  const float descale[3] = {q_descale, k_descale, v_descale};
+  return launch_fwd_tc<128, false, true>(q, k, v, o, lse, B, Hq, Hkv, T, S, causal, key_lens,
+                                         nullptr, scale, reinterpret_cast<cudaStream_t>(stream),
+                                         descale);
 }
 
 int attn_fwd_chunked(const void* q, const void* kcache, const void* vcache, void* o, float* lse,

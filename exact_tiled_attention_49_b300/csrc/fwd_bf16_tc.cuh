@@ -56,13 +56,18 @@ constexpr int kThreads = 320;         // 8 softmax warps + MMA warp + load warp
 constexpr float kRescaleThreshold = 8.0f;
 constexpr uint32_t kTmemCols = 512;
 
-template <int D>
+// EB: bytes per input element (2: bf16 / fp16, 1: E4M3).
+template <int D, int EB = 2>
 struct Cfg {
-  static constexpr int kChunks = D / 64;                    // 64-column (128 B) chunks
-  static constexpr uint32_t kTileBytes = kBN * D * 2;       // one K or V tile
+  static constexpr int kRowBytes = D * EB;                  // one Q, K or V row
+  static constexpr int kChunks = kRowBytes / 128;           // 128-byte swizzle chunks per row
+  static constexpr int kChunkElems = 128 / EB;              // elements of a chunk row
+  static constexpr uint32_t kTileBytes = kBN * kRowBytes;   // one K or V tile
   static constexpr uint32_t kChunkBytes = kBN * 128;        // 128 rows x 128 B
-  static constexpr uint32_t kQBytes = kBM * D * 2;          // one query tile
-  static constexpr int kSlots = (D == 128) ? 5 : 8;
+  static constexpr uint32_t kQBytes = kBM * kRowBytes;      // one query tile
+  static constexpr int kKSteps = kRowBytes / 32;            // S = Q K^T: 32-byte K steps
+  static constexpr int kPvSteps = kBN * EB / 64;            // P V per 64-key half: 32-byte steps
+  static constexpr int kSlots = (kTileBytes >= 32768) ? 5 : 8;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffSlots = kQTiles * kQBytes;
   static constexpr uint32_t kOffBars = kOffSlots + kSlots * kTileBytes;
@@ -89,7 +94,8 @@ struct Params {
                             // when a sequence's pairs may be shifted
   int n_items;              // n_pairs * B * Hq
   int o_align32;            // o is 32-byte aligned: 256-bit stores
-  float scale_log2;         // scale * log2(e)
+  float scale_log2;         // scale * log2(e) (E4M3: times the Q and K descales)
+  float o_scale;            // factor on O (E4M3: the V descale; else 1)
   FastDiv div_B, div_Hq, div_G;  // division by B, Hq and Hq / Hkv
 };
 
@@ -286,12 +292,21 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 }
 
 // kF16: fp16 inputs and output (else bf16); both use kind::f16 MMAs.
-template <int D, bool kF16>
+// kF8: E4M3 inputs (kind::f8f6f4 MMAs, P rounded to E4M3 for P V), bf16
+// output.  P is formed against a reference 7 below the row maximum's
+// (P' = 2^7 P), so the weights that matter stay in E4M3's normal range (down
+// to 2^-13 of the largest); with the lazy-rescale threshold at 1 the largest
+// P' is 2^8 < 448.  O / l and the LSE use the same biased reference, so the
+// bias cancels exactly.
+template <int D, bool kF16, bool kF8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, Params p) {
-  using C = Cfg<D>;
+  static_assert(!(kF16 && kF8), "E4M3 inputs write bf16 output");
+  using C = Cfg<D, kF8 ? 1 : 2>;
+  constexpr float kPBias = kF8 ? 7.f : 0.f;                      // log2 of P's scale
+  constexpr float kThresh = kF8 ? 1.f : kRescaleThreshold;       // lazy-rescale threshold
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -391,8 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           mbar_arrive_expect_tx(bar_qfull(t), C::kQBytes);
           for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(s_q + t * C::kQBytes + c * C::kChunkBytes, &tm_q, bar_qfull(t), c * 64,
-                        x.q0 + t * kBM, x.b * p.Hq + x.h);
+            tma_load_3d(s_q + t * C::kQBytes + c * C::kChunkBytes, &tm_q, bar_qfull(t),
+                        c * C::kChunkElems, x.q0 + t * kBM, x.b * p.Hq + x.h);
         }
       }
     };
@@ -412,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         mbar_arrive_expect_tx(bar_land, C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(dst + c * C::kChunkBytes, tm, bar_land, c * 64, row, bh_kv);
+          tma_load_3d(dst + c * C::kChunkBytes, tm, bar_land, c * C::kChunkElems, row, bh_kv);
       }
       if (tail) {
         ok = wait_bar(bar_tail, ntail & 1);
@@ -474,8 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp walks the schedule; one elected lane issues each
     // tcgen05 instruction.  Descriptors are built once per base address and
     // advanced by constants, so every MMA costs only its issue slot.
-    constexpr uint32_t idesc_qk = idesc_f16kind(kBM, kBN, false, false, kF16);
-    constexpr uint32_t idesc_pv = idesc_f16kind(kBM, D, false, true, kF16);
+    constexpr uint32_t idesc_qk =
+        kF8 ? idesc_e4m3(kBM, kBN, false, false) : idesc_f16kind(kBM, kBN, false, false, kF16);
+    constexpr uint32_t idesc_pv =
+        kF8 ? idesc_e4m3(kBM, D, false, true) : idesc_f16kind(kBM, D, false, true, kF16);
     const uint64_t dq0 = sdesc_sw128(s_q, 16, 1024);                // Q_0 as the A operand
     const uint64_t dk0 = sdesc_sw128(s_slots, 16, 1024);            // slot 0 as K (K-major B)
     const uint64_t dv0 = sdesc_sw128(s_slots, C::kChunkBytes, 1024);  // slot 0 as V (MN-major B)
@@ -497,20 +514,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dq = dq0 + (uint64_t)((t * C::kQBytes) >> 4);
       const uint64_t dk = dk0 + (uint64_t)((slot * C::kTileBytes) >> 4);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
+      for (int kk = 0; kk < C::kKSteps; ++kk) {
         const uint32_t koff = ((kk >> 2) * C::kChunkBytes + (kk & 3) * 32) >> 4;
-        umma_ss_elect(tmem + C::kColS(t), dq + koff, dk + koff, idesc_qk, kk > 0);
+        if constexpr (kF8)
+          umma_ss_elect_f8(tmem + C::kColS(t), dq + koff, dk + koff, idesc_qk, kk > 0);
+        else
+          umma_ss_elect(tmem + C::kColS(t), dq + koff, dk + koff, idesc_qk, kk > 0);
       }
       umma_commit_elect(bar_s + 8 * t);
     };
-    // O_t += P_t V for keys [64 * half, 64 * half + 64) of the tile in `slot`.
+    // O_t += P_t V for keys [64 * half, 64 * half + 64) of the tile in `slot`:
+    // each step takes 32 bytes of P's row (8 TMEM columns) and 32 bytes' worth
+    // of V rows (256 / EB bytes >> 4 further into the MN-major tile).
     auto issue_pv = [&](int t, int slot, int half, bool acc) {
       const uint64_t dv = dv0 + (uint64_t)((slot * C::kTileBytes) >> 4);
 #pragma unroll
-      for (int k4 = 0; k4 < kBN / 32; ++k4) {
-        const int kk = half * (kBN / 32) + k4;
-        umma_ts_elect(tmem + C::kColO(t), tmem + C::kColS(t) + kk * 8, dv + (uint64_t)(kk * 128),
-                      idesc_pv, (acc || kk > 0) ? 1u : 0u);
+      for (int k4 = 0; k4 < C::kPvSteps; ++k4) {
+        const int kk = half * C::kPvSteps + k4;
+        const uint64_t bo = (uint64_t)(kk * (kF8 ? 256 : 128));
+        if constexpr (kF8)
+          umma_ts_elect_f8(tmem + C::kColO(t), tmem + C::kColS(t) + kk * 8, dv + bo, idesc_pv,
+                           (acc || kk > 0) ? 1u : 0u);
+        else
+          umma_ts_elect(tmem + C::kColO(t), tmem + C::kColS(t) + kk * 8, dv + bo, idesc_pv,
+                        (acc || kk > 0) ? 1u : 0u);
       }
     };
     // Next item with key tiles to visit and its tile counts (false when the
@@ -682,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             sl2;  // -inf stays -inf
         // Lazy rescale: move the reference only when the maximum ran ahead.
         const bool first = (m_ref == -INFINITY);
-        const bool grow = !first && (m_tile > m_ref + kRescaleThreshold);
+        const bool grow = !first && (m_tile > m_ref + kThresh);
         float alpha = 1.f;
         if (first && m_tile != -INFINITY) m_ref = m_tile;
         if (grow) {
@@ -693,11 +720,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         // P = exp2(s * scale * log2e - m_ref), packed to bf16 pairs, in two
         // halves of 64 keys; each half is released to the MMA warp on its own.
-        const float neg_ref = (m_ref == -INFINITY) ? 0.f : -m_ref;
+        const float neg_ref = (m_ref == -INFINITY) ? 0.f : kPBias - m_ref;
         const float2 sl2x2 = make_float2(sl2, sl2);
         const float2 negx2 = make_float2(neg_ref, neg_ref);
         float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
-        uint32_t pk[kBN / 2];
+        uint32_t pk[kBN / 2];  // E4M3: the first kBN / 4 words
+        float2 pprev = acc0;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
 #pragma unroll
@@ -708,14 +736,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                   make_float2(__uint_as_float(sr[c + e]), __uint_as_float(sr[c + e + 1])), sl2x2,
                   negx2);
               const float2 pe = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-              pk[(c + e) >> 1] = pack2<kF16>(pe.x, pe.y);
+              if constexpr (kF8) {
+                if (e & 2) pk[(c + e) >> 2] = pack_e4m3x4(pprev.x, pprev.y, pe.x, pe.y);
+                else pprev = pe;
+              } else {
+                pk[(c + e) >> 1] = pack2<kF16>(pe.x, pe.y);
+              }
               if (e == 0) acc0 = __fadd2_rn(acc0, pe);
               else if (e == 2) acc1 = __fadd2_rn(acc1, pe);
               else if (e == 4) acc2 = __fadd2_rn(acc2, pe);
               else acc3 = __fadd2_rn(acc3, pe);
             }
           }
-          tmem_st32(ts + 32 * half, pk + 32 * half);
+          if constexpr (kF8) tmem_st16(ts + 16 * half, pk + 16 * half);
+          else tmem_st32(ts + 32 * half, pk + 32 * half);
           if (half == 0) {
             // O_t is final up to key tile j-1 here: PV_t(j-1) was issued
             // before S_t(j), whose completion this group has seen.  PV_t(j)
@@ -752,23 +786,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
       }
       const bool has = row_ok && (l > 0.f);
-      const float inv = has ? 1.f / l : 0.f;
+      const float inv = has ? p.o_scale / l : 0.f;
       uint16_t* orow =
           reinterpret_cast<uint16_t*>(p.o) + ((((size_t)it.b * p.Hq + it.h) * p.T) + i) * D;
       if (__any_sync(0xffffffffu, has)) {
         tc_fence_after();
+        // 64 columns at a time; the next chunk's TMEM load is issued before
+        // this chunk's stores so its latency overlaps them.
+        uint32_t orr[64];
+        tmem_ld32(to, orr);
+        tmem_ld32(to + 32, orr + 32);
+        tmem_wait_ld32(orr);
+        tmem_wait_ld32(orr + 32);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
-          uint32_t orr[64];
-          tmem_ld32(to + 64 * c, orr);
-          tmem_ld32(to + 64 * c + 32, orr + 32);
-          tmem_wait_ld32(orr);
-          tmem_wait_ld32(orr + 32);
           uint32_t pkd[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e)
             pkd[e] = pack2<kF16>(__uint_as_float(orr[2 * e]) * inv,
                                  __uint_as_float(orr[2 * e + 1]) * inv);
+          if (c + 1 < D / 64) {
+            tmem_ld32(to + 64 * (c + 1), orr);
+            tmem_ld32(to + 64 * (c + 1) + 32, orr + 32);
+          }
           if (i >= 0 && i < p.T) {
             uint16_t* dst = orow + 64 * c;
             if (p.o_align32) {
@@ -781,6 +821,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     make_uint4(pkd[4 * v], pkd[4 * v + 1], pkd[4 * v + 2], pkd[4 * v + 3]);
             }
           }
+          if (c + 1 < D / 64) {
+            tmem_wait_ld32(orr);
+            tmem_wait_ld32(orr + 32);
+          }
         }
         tc_fence_before();
       } else if (i >= 0 && i < p.T) {
@@ -789,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (p.lse != nullptr && i >= 0 && i < p.T) {
         p.lse[((size_t)it.b * p.Hq + it.h) * p.T + i] =
-            has ? (m_ref + __log2f(l)) * 0.69314718055994531f : -INFINITY;
+            has ? (m_ref - kPBias + __log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
     }
     // Items with no key tile: every row is padded (or past T): O = 0, LSE = -inf.

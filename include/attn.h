@@ -101,6 +101,34 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
              attn_stream_t stream);
 
 /*
+ * attn_fwd_fp8 -- attn_fwd on FP8 E4M3 inputs ("Self-Attention:
+ * Implementation, Complexity, and Efficient Variants", FlashAttention-3: FP8
+ * support).  The attention of the dequantised inputs
+ *     q = q_descale * Q8,  k = k_descale * K8,  v = v_descale * V8
+ * with the masks, scale, GQA mapping and outputs of attn_fwd.  Scores are
+ * exact products of the E4M3 values accumulated in fp32 (tcgen05
+ * kind::f8f6f4); the softmax weights are rounded to E4M3 for P V (formed
+ * as 2^7 times the weights relative to a running reference, so every weight
+ * down to 2^-13 of the row's largest keeps E4M3's 3-bit mantissa); the
+ * row sums and the LSE use the unrounded fp32 weights.
+ *
+ *   q                 [B,Hq,T,128]   E4M3 bytes     (read)
+ *   k, v              [B,Hkv,S,128]  E4M3 bytes     (read)
+ *   o                 [B,Hq,T,128]   bf16           (written)
+ *   lse               [B,Hq,T]       float32        (written; NULL = do not emit)
+ *   key_lens          [B]            int32, device  (NULL = all S keys valid)
+ *   q_descale, k_descale, v_descale: finite, > 0
+ *
+ * Supported: D = 128 (else ATTN_ERR_UNSUPPORTED); q, k, v, o 16-byte
+ * aligned.  Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED or
+ * ATTN_ERR_CUDA.
+ */
+ATTN_API int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int Hq, int Hkv, int T, int S, int D, int causal,
+                          const int32_t* key_lens, float scale, float q_descale,
+                          float k_descale, float v_descale, attn_stream_t stream);
+
+/*
  * attn_fwd_chunked -- chunked prefill against a KV cache: a chunk of up to T
  * new queries per sequence attends over that sequence's cache, which already
  * holds the chunk's own K/V rows (append them first, e.g. with one copy per
