@@ -234,10 +234,19 @@ def decode_flops(Hq, D, kv_lens):
     return 4.0 * Hq * D * float(sum(int(x) for x in kv_lens))
 
 
-def build_case(wid, device, batch=None, backward=False):
+def quantize_e4m3(t):
+    """Per-tensor E4M3 quantisation (descale = amax / 256): (fp8 tensor, descale)."""
+    import torch
+    x = t.float()
+    d = float(x.abs().max()) / 256.0
+    return (x / d).to(torch.float8_e4m3fn), d
+
+
+def build_case(wid, device, batch=None, backward=False, fp8=False):
     """Device tensors for one step of workload `wid` and its bookkeeping.
     With `backward`, the step is the backward pass of the prefill (its O and
-    LSE computed once, outside the timed region)."""
+    LSE computed once, outside the timed region); with `fp8`, the prefill on
+    the inputs quantised to E4M3 per tensor (quantised once, outside)."""
     import torch
     import workloads
     w = workloads.workload(wid, batch)
@@ -249,6 +258,13 @@ def build_case(wid, device, batch=None, backward=False):
         case["lse"] = torch.empty(w.B, w.Hq, w.T, device=device, dtype=torch.float32)
         kl = None if x["key_lens"] is None else x["key_lens"].cpu().numpy()
         case["flops"] = prefill_flops(w, kl)
+        if fp8:
+            f = {}
+            for n in ("q", "k", "v"):
+                f[n], f["d" + n] = quantize_e4m3(x[n])
+            case["fp8"] = f
+            case["o"] = torch.empty(x["q"].shape, dtype=torch.bfloat16, device=device)
+            return case
         if backward:
             import exact_tiled_attention_49_b300 as E
             scale = 1.0 / math.sqrt(w.D)
@@ -309,6 +325,13 @@ def step_groups(c):
     w = c["w"]
     scale = 1.0 / math.sqrt(w.D)
     groups = []
+    if "fp8" in c:
+        f = c["fp8"]
+        groups.append(("prefill", lambda: E.attn_fwd_fp8(
+            f["q"], f["k"], f["v"], o=c["o"], lse=c["lse"], causal=w.causal,
+            key_lens=c["key_lens"], scale=scale, q_descale=f["dq"], k_descale=f["dk"],
+            v_descale=f["dv"])))
+        return groups
     if "bwd" in c:
         bw = c["bwd"]
         groups.append(("prefill", lambda: E.attn_bwd(
@@ -555,14 +578,20 @@ def run_e2e(E, c, steps, device):
     the step's inputs, the step, D2H copy of its outputs, all timed."""
     import torch
     w = c["w"]
-    if "bwd" in c:
-        # backward: inputs q, k, v, dO, O, LSE; results dQ, dK, dV
-        bw = c["bwd"]
-        dev_in = {"q": c["q"], "k": c["k"], "v": c["v"], "do": bw["do"], "o": bw["o"],
-                  "lse": bw["lse"]}
+    if "bwd" in c or "fp8" in c:
+        if "bwd" in c:
+            # backward: inputs q, k, v, dO, O, LSE; results dQ, dK, dV
+            bw = c["bwd"]
+            dev_in = {"q": c["q"], "k": c["k"], "v": c["v"], "do": bw["do"], "o": bw["o"],
+                      "lse": bw["lse"]}
+            dev_out = [bw[n] for n in ("dq", "dk", "dv")]
+        else:
+            # E4M3 prefill: inputs the quantised q, k, v; results O, LSE
+            f = c["fp8"]
+            dev_in = {n: f[n] for n in ("q", "k", "v")}
+            dev_out = [c["o"], c["lse"]]
         host_in = {n: t.cpu().pin_memory() for n, t in dev_in.items()}
-        outs = [(torch.empty(bw[n].shape, dtype=bw[n].dtype).pin_memory(), bw[n])
-                for n in ("dq", "dk", "dv")]
+        outs = [(torch.empty(t.shape, dtype=t.dtype).pin_memory(), t) for t in dev_out]
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = sum(h.numel() * h.element_size() for h, _ in outs)
         s0 = torch.cuda.Event(enable_timing=True)
@@ -732,9 +761,11 @@ def bench_ours(args):
     import exact_tiled_attention_49_b300 as E
     E.load()
     peaks = load_peaks()
-    if args.backward and workloads_kind(args.workload) != "prefill":
-        raise SystemExit("--backward needs a prefill workload (2, 3 or 5)")
-    c = build_case(args.workload, device, args.batch, backward=args.backward)
+    if (args.backward or args.fp8) and workloads_kind(args.workload) != "prefill":
+        raise SystemExit("--backward and --fp8 need a prefill workload (2, 3 or 5)")
+    if args.backward and args.fp8:
+        raise SystemExit("--backward and --fp8 are separate modes")
+    c = build_case(args.workload, device, args.batch, backward=args.backward, fp8=args.fp8)
     w = c["w"]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     for _ in range(args.warmup):
@@ -770,12 +801,21 @@ def bench_ours(args):
                     prefill_flops(w, None if c["key_lens"] is None else c["key_lens"].cpu().numpy())
                     ) / (kern_ms["prefill"] * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
-        out["roofline"] = {"kernel": ("bwd_delta_kernel+bwd_dq_kernel+bwd_dkdv_kernel"
-                                      if "bwd" in c else "fwd_bf16_tc_kernel"), "bound": "tensor",
+        kernel = ("bwd_delta_kernel+bwd_dq_kernel+bwd_dkdv_kernel" if "bwd" in c else
+                  "fwd_bf16_tc_kernel<128,0,1>" if "fp8" in c else "fwd_bf16_tc_kernel")
+        peak_source = peaks["source"] + " bf16 burst"
+        if "fp8" in c:
+            # a contraction takes the peak of its own type: the measured bf16
+            # burst times the nominal FP8 / bf16 ratio (4.5 / 2.25 PFLOP/s)
+            peak *= 2.0
+            peak_source += " x 2 (nominal FP8/bf16 ratio)"
+            out["dtype"] = "e4m3"
+        traffic = (profiled_traffic(args.workload)
+                   if args.batch is None and not args.backward and not args.fp8 else None)
+        out["roofline"] = {"kernel": kernel, "bound": "tensor",
                            "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                           "frac": achieved / peak,
-                           "traffic": profiled_traffic(args.workload) if args.batch is None else None,
-                           "peak_source": peaks["source"] + " bf16 burst"}
+                           "frac": achieved / peak, "traffic": traffic,
+                           "peak_source": peak_source}
         if "dec" in c:
             gbs = c["dec_bytes"] / (kern_ms["decode"] * 1e-3) / 1e9
             out["decode"] = {"workload": "next-token decode of the same batch (kv_len 1025)",
@@ -793,7 +833,9 @@ def bench_ours(args):
                            "traffic": profiled_traffic(args.workload) if args.batch is None else None,
                            "peak_source": peaks["source"] + " HBM copy"}
     cfg = {"workload": ("backward (dQ, dK, dV, 2.5x the forward's FLOPs) of: " + w.name
-                        if "bwd" in c else w.name), "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                        if "bwd" in c else
+                        "E4M3 inputs (per-tensor descales): " + w.name if "fp8" in c else w.name),
+           "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
            "l2": "flushed between steps (256 MiB write, outside the timed events)",
            "timing": "CUDA events around CUDA-graph replays of each kernel group of the step",
            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
@@ -874,6 +916,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (dQ, dK, dV) of the prefill workload instead")
+    ap.add_argument("--fp8", action="store_true",
+                    help="time the prefill workload on E4M3 inputs (attn_fwd_fp8) instead")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip timing the other benchmark workloads")
     ap.add_argument("--batch", type=int, default=None,

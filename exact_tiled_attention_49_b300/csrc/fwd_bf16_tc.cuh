@@ -578,13 +578,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       first_qk(1, n1, kslot0);
       umma_commit_elect(bar_empty(kslot0));
+      // The next item is walked after step 0's products are issued (the walk
+      // costs this warp ~2000 cycles; there it overlaps the softmax of step 1).
       int nn0 = 0, nn1 = 0;
-      const bool have_nx = next_item(nn0, nn1);
-      // Causal diagonal: tile 1 visits one key tile more than tile 0.  Once
-      // tile 0 is done (step n0 - 1) the next item's S_0(0) is issued from its
-      // K_0, which the load warp placed between this item's last K and V, so
-      // the tensor core is busy while tile 1 finishes alone.
-      const bool early_next = have_nx && n0 >= 1 && n1 == n0 + 1;
+      bool have_nx = false, early_next = false;
       early = false;
       for (int j = 0; ok && j < nm; ++j) {
         const int vslot = ring % C::kSlots;
@@ -626,6 +623,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           // K_{j+1} is consumed by at least one tile because j + 1 < nm.
           umma_commit_elect(bar_empty(kslot));
           ++ring;
+        }
+        if (j == 0) {
+          have_nx = next_item(nn0, nn1);
+          // Causal diagonal: tile 1 visits one key tile more than tile 0.  Once
+          // tile 0 is done (step n0 - 1) the next item's S_0(0) is issued from
+          // its K_0, which the load warp placed between this item's last K and
+          // V, so the tensor core is busy while tile 1 finishes alone.
+          early_next = have_nx && n0 >= 1 && n1 == n0 + 1;
         }
         if (early_next && j == n0 - 1) {
           // Q_0 and K_0 of the next item (qi already counts this item)
