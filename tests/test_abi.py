@@ -119,3 +119,42 @@ def test_append_rejects_bad_arguments(lib):
 
 def test_launch_counter_is_host_side(lib):
     assert isinstance(lib.attn_kernel_launches(), int)
+
+
+def test_fwd_fp8_rejects_bad_arguments(lib):
+    def f8(q=FAKE, D=128, Hq=2, Hkv=1, qd=0.5, kd=0.5, vd=0.5, scale=0.125):
+        return lib.attn_fwd_fp8(q, FAKE, FAKE, FAKE, None, 1, Hq, Hkv, 8, 8, D, 1, None, scale,
+                                qd, kd, vd, None)
+    assert f8(q=None) == 1
+    assert f8(Hq=3, Hkv=2) == 1
+    assert f8(qd=0.0) == 1                 # descales must be finite and > 0
+    assert f8(vd=float("nan")) == 1
+    assert f8(kd=-1.0) == 1
+    assert f8(scale=float("inf")) == 1
+    assert f8(D=64) == 2                   # E4M3 rows must be one 128-byte swizzle row
+    assert f8(q=MIS) == 1
+
+
+def test_fwd_chunked_rejects_bad_arguments(lib):
+    def ch(q_pos=FAKE, kv_lens=FAKE, D=64, dt=1):
+        return lib.attn_fwd_chunked(FAKE, FAKE, FAKE, FAKE, None, q_pos, kv_lens, 1, 1, 1, 8, 16,
+                                    D, dt, 1, 0.125, None)
+    assert ch(q_pos=None) == 1             # q_pos and kv_lens are required
+    assert ch(kv_lens=None) == 1
+    assert ch(D=96) == 2
+    assert ch(dt=7) == 1
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    need = lib.attn_bwd_workspace_size(1, 2, 8)
+    assert need >= 2 * 8 * 4               # one fp32 delta per query row
+
+    def bw(dq=FAKE, D=64, dt=1, ws=FAKE, ws_bytes=need, Hq=2, Hkv=1):
+        return lib.attn_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, dq, FAKE, FAKE, 1, Hq, Hkv, 8, 8, D,
+                            dt, 1, None, None, 0.125, ws, ws_bytes, None)
+    assert bw(dq=None) == 1
+    assert bw(Hq=3, Hkv=2) == 1
+    assert bw(dt=0) == 2                   # fp32 backward is not built
+    assert bw(D=96) == 2
+    assert bw(ws=None) == 3
+    assert bw(ws_bytes=need - 4) == 3
