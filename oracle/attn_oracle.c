@@ -29,7 +29,7 @@
  *  - "FlashAttention" (Transformers in Action, section 9.4.1): the tiled
  *      method is exact, so the plain definition is the oracle.
  *
- * Readings where the pages are silent (each also listed in the design doc):
+ * Readings where the pages are silent:
  *  - Causal alignment is bottom-right: query i sits at key position
  *    i + (S - T); visible(i,j) = (j < L) and (not causal or j <= i + S - T).
  *  - key_lens[b] = L gives the valid length of sequence b for keys AND
