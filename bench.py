@@ -73,10 +73,10 @@ PROFILED_TRAFFIC = {
     5: {"source": "exact_tiled_attention_49_b300/csrc/fwd_bf16_tc.cuh", "sha256": "546236c13a29",
         "bytes": 1.08075e9 + 89.931008e6, "scale": 1.0,
         "capture": "fwd_bf16_tc_kernel<128,0,0>, full workload"},
-    4: {"source": "exact_tiled_attention_49_b300/csrc/decode.cuh", "sha256": "b95870e96e87",
-        "bytes": 360.429568e6 + 6.840064e6, "scale": 1333948416.0 / 358866944.0,
-        "capture": "decode_split_mma_kernel, profiling case B=16 of workload 4, scaled by "
-                   "the algorithmic K/V bytes (full / captured)"},
+    4: {"source": "exact_tiled_attention_49_b300/csrc/decode.cuh", "sha256": "7f25a6c1b376",
+        "bytes": 1.342135e9 + 23.034368e6, "scale": 1.0,
+        "capture": "decode_split_mma_kernel<128,4,0>, full workload"},
+
 }
 
 
