@@ -76,7 +76,6 @@ PROFILED_TRAFFIC = {
     4: {"source": "exact_tiled_attention_49_b300/csrc/decode.cuh", "sha256": "7f25a6c1b376",
         "bytes": 1.342135e9 + 23.034368e6, "scale": 1.0,
         "capture": "decode_split_mma_kernel<128,4,0>, full workload"},
-
 }
 
 
