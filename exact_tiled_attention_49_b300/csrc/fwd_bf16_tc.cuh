@@ -1,5 +1,5 @@
-// fwd_bf16_tc.cuh -- bf16 / fp16 prefill forward on the 5th-generation tensor
-// cores.
+// fwd_bf16_tc.cuh -- bf16 / fp16 / E4M3 prefill forward on the 5th-generation
+// tensor cores.
 //
 // The method ("FlashAttention", Transformers in Action section 9.4.1 and
 // Figure 9.8; "Implementing attention from scratch", Core ideas, Stable
@@ -8,10 +8,12 @@
 // the partial output is rescaled by exp(m_old - m_new) when m grows, so the
 // T x S score matrix never reaches HBM.
 //
-// Mapping to sm_103a.  The kernel is persistent: CTA c handles work items
-// c, c + gridDim.x, ...; an item is a pair of 128-row query tiles (rows q0 ..
-// q0 + 255) of one (batch, head), and items are numbered heaviest first so
-// that causal work balances over the SMs.  Per CTA:
+// Mapping to sm_103a.  The kernel is persistent, one CTA per SM; an item is a
+// pair of 128-row query tiles (rows q0 .. q0 + 255) of one (batch, head),
+// paired from the top of the sequence's non-padded rows (so q0 may be -128:
+// a virtual first tile), and the items, numbered heaviest first, are dealt
+// to the CTAs in snake order so that causal work balances over the SMs
+// (sched_next).  Per CTA:
 //   warps 0-3   softmax of query tile 0, warps 4-7 softmax of query tile 1:
 //               thread r of a group owns TMEM lane r = query row r of its
 //               tile.  It loads its 128 scores, masks diagonal/boundary tiles
@@ -24,6 +26,10 @@
 //               O_t += P_t V_j with P_t read from TMEM as the A operand.
 //   warp 9      TMA producer: Q_0, Q_1 once per item, then K_0, V_0, K_1,
 //               V_1, ... into a ring of 128B-swizzled shared-memory slots.
+//               With a causal diagonal (tile 1 visits one key tile more) the
+//               next item's Q_0 and K_0 go out between this item's last K
+//               and last V, and the MMA warp starts the next item's S_0
+//               while tile 1 finishes alone.
 // The two query tiles share every K/V tile and take turns on the tensor
 // cores: while group 0 turns S_0 into P_0, the tensor cores compute P_1 V and
 // the next S_1, and the other way round.  Issue order per key tile j:
@@ -36,7 +42,8 @@
 // Rescaling is lazy: the exponent reference m_ref moves only when a row's
 // maximum exceeds it by more than kRescaleThreshold (log2 units), so P can
 // reach 2^8 but O, l and m_ref always stay consistent and the final O / l is
-// exact up to rounding.
+// exact up to rounding.  E4M3 inputs use kind::f8f6f4 MMAs and round P to
+// E4M3 (see the kF8 notes at the kernel).
 #pragma once
 
 #include <cuda.h>
