@@ -64,13 +64,13 @@ def load_peaks():
 # "scale" converts the captured launch to a full launch of the bench
 # workload by the units it processes (1.0 when captured at full size).
 PROFILED_TRAFFIC = {
-    2: {"source": "exact_tiled_attention_49_b300/csrc/fwd_bf16_tc.cuh", "sha256": "546236c13a29",
+    2: {"source": "exact_tiled_attention_49_b300/csrc/fwd_bf16_tc.cuh", "sha256": "365975bf826d",
         "bytes": 12.657408e6 + 0.0, "scale": 1.0,
         "capture": "fwd_bf16_tc_kernel<64,0,0>, full workload (the default step's prefill)"},
-    3: {"source": "exact_tiled_attention_49_b300/csrc/fwd_bf16_tc.cuh", "sha256": "546236c13a29",
+    3: {"source": "exact_tiled_attention_49_b300/csrc/fwd_bf16_tc.cuh", "sha256": "365975bf826d",
         "bytes": 2.169796e9 + 118.461696e6, "scale": 1.0,
         "capture": "fwd_bf16_tc_kernel<128,0,0>, full workload"},
-    5: {"source": "exact_tiled_attention_49_b300/csrc/fwd_bf16_tc.cuh", "sha256": "546236c13a29",
+    5: {"source": "exact_tiled_attention_49_b300/csrc/fwd_bf16_tc.cuh", "sha256": "365975bf826d",
         "bytes": 1.08075e9 + 89.931008e6, "scale": 1.0,
         "capture": "fwd_bf16_tc_kernel<128,0,0>, full workload"},
     4: {"source": "exact_tiled_attention_49_b300/csrc/decode.cuh", "sha256": "7f25a6c1b376",
