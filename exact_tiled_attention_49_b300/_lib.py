@@ -38,6 +38,7 @@ SIGNATURES = {
     "attn_status_string": (ctypes.c_char_p, [_I]),
     "attn_kernel_launches": (ctypes.c_ulonglong, []),
     "attn_device_error": (_I, [ctypes.POINTER(ctypes.c_int), _I]),
+    "attn_selftest_wait_timeout": (_I, [_P]),
 }
 
 
@@ -367,6 +368,15 @@ def kv_cache_append(kcache, vcache, k_new, v_new, pos, dev_status=None, stream=N
 
 def attn_kernel_launches() -> int:
     return int(load().attn_kernel_launches())
+
+
+ATTN_SELFTEST_ERROR = 0x1EE  # 0x100 (wait timed out) | site 0xEE
+
+
+def attn_selftest_wait_timeout(stream=None) -> None:
+    """Launch the bounded-wait self test (see include/attn.h); the error it
+    records is read with attn_device_error()."""
+    _check(load().attn_selftest_wait_timeout(_stream(stream)), "attn_selftest_wait_timeout")
 
 
 def attn_device_error(clear: bool = True) -> int:

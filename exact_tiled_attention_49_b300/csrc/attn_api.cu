@@ -382,6 +382,23 @@ int fwd_dispatch(const void* q, const void* k, const void* v, void* o, float* ls
 
 }  // namespace
 
+namespace attn {
+// One warp waits on a barrier that no thread arrives at: the bounded wait
+// must give up, record its site in the error word and let the kernel return.
+__global__ void selftest_wait_kernel() {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncwarp();
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, 0xEE, &abort_flag);
+  __syncwarp();
+}
+}  // namespace attn
+
 extern "C" {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
@@ -603,6 +620,11 @@ const char* attn_status_string(int status) {
 }
 
 unsigned long long attn_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int attn_selftest_wait_timeout(attn_stream_t stream) {
+  attn::selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>();
+  return launch_status();
+}
 
 int attn_device_error(int* code, int clear) {
   int v = 0;

@@ -324,9 +324,18 @@ ATTN_API const char* attn_status_string(int status);
  *   error word, which a kernel sets instead of trapping when an internal
  *   pipeline wait exceeds its time limit.  0 means no error.  Synchronises
  *   the device.  Returns ATTN_OK or ATTN_ERR_CUDA.
+ *
+ * attn_selftest_wait_timeout -- checks the failure path of those waits:
+ *   launches one warp that waits on a shared-memory barrier nothing will
+ *   complete.  The wait gives up after its time limit (about one second),
+ *   records ATTN_SELFTEST_ERROR in the device error word (unless an earlier
+ *   error is already there) and returns; the context stays usable.  Returns
+ *   ATTN_OK or ATTN_ERR_CUDA (launch status only).
  */
+#define ATTN_SELFTEST_ERROR 0x1EE /* 0x100 (wait timed out) | site 0xEE */
 ATTN_API unsigned long long attn_kernel_launches(void);
 ATTN_API int attn_device_error(int* code, int clear);
+ATTN_API int attn_selftest_wait_timeout(attn_stream_t stream);
 
 #ifdef __cplusplus
 }
