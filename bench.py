@@ -3,19 +3,23 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2|3|4|5]
                     [--impl ours|reference]
 
-Default workload 2, causal self-attention prefill B=4 H=8 T=S=1024 D=64 bf16:
-one step is one pass of the hot path over that batch, i.e. the prefill
-forward (O and LSE), then appending the next token's K/V to a KV cache that
-holds the prompt and one decode step for it.  Workloads 3 and 5 time the
-prefill forward alone; workload 4 times append + decode.  Inputs are seeded
-synthetic tensors already resident in HBM; L2 is flushed (256 MiB write)
-between timed steps, outside the timed events.
+Default workload 3, long-context causal prefill B=1 H=16 T=S=32768 D=128
+bf16 with Q x 2: one step is one prefill forward (O and LSE) over that
+sequence.  The line also carries a ``decode`` block for workload 4, the GQA
+KV-cache decode step (B=64, Hq=32, Hkv=8, D=128, cache lengths U[1024,8192]:
+append the new token's K/V, then decode), with its own roofline, end-to-end
+figure and CPU baseline: the metric names both halves.  ``--workload 2``
+times the short causal prefill plus the next-token append and decode of the
+same batch; ``--workload 5`` the padded batch prefill; ``--workload 4`` the
+decode step alone.  Inputs are seeded synthetic tensors already resident in
+HBM; L2 is flushed (256 MiB write) between timed steps, outside the timed
+events.
 
 Printed: ONE JSON line (rank 0) with the metric, whole-job throughput, the
 roofline of the dominant kernel (its own CUDA-event time), an end-to-end
-figure through the public API with host buffers, the float64 CPU oracle timed
-on the host cores, SM clocks sampled during the timed region and the number
-of library kernels launched.
+figure through the public API with host buffers (with its copy / call
+breakdown), the float64 CPU oracle timed on the host cores, SM clocks sampled
+during the timed region and the number of library kernels launched.
 
 ``--impl reference`` times the float64 CPU oracle (the reference arm; there
 is no installable reference implementation) on bounded samples of the same
@@ -121,9 +125,65 @@ def barrier(ws: int):
         dist.barrier()
 
 
+class _NvmlCtypes:
+    """The few NVML calls the clock sampler needs, bound with ctypes to the
+    driver's libnvidia-ml.so.1 (for hosts where the pynvml module is not
+    importable).  Same method names and results as pynvml's."""
+
+    NVML_CLOCK_SM = 1
+
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        self._chk(self.lib.nvmlInit_v2())
+
+    def _chk(self, rc):
+        if rc != 0:
+            raise RuntimeError(f"NVML error {rc}")
+
+    def nvmlInit(self):
+        pass
+
+    def nvmlDeviceGetHandleByPciBusId(self, bus):
+        h = self.ct.c_void_p()
+        self._chk(self.lib.nvmlDeviceGetHandleByPciBusId_v2(self.ct.c_char_p(bus),
+                                                            self.ct.byref(h)))
+        return h
+
+    def nvmlDeviceGetHandleByIndex(self, i):
+        h = self.ct.c_void_p()
+        self._chk(self.lib.nvmlDeviceGetHandleByIndex_v2(self.ct.c_uint(i), self.ct.byref(h)))
+        return h
+
+    def nvmlDeviceGetIndex(self, h):
+        v = self.ct.c_uint()
+        self._chk(self.lib.nvmlDeviceGetIndex(h, self.ct.byref(v)))
+        return v.value
+
+    def _clock(self, fn, h, typ):
+        v = self.ct.c_uint()
+        self._chk(fn(h, self.ct.c_int(typ), self.ct.byref(v)))
+        return v.value
+
+    def nvmlDeviceGetMaxClockInfo(self, h, typ):
+        return self._clock(self.lib.nvmlDeviceGetMaxClockInfo, h, typ)
+
+    def nvmlDeviceGetClockInfo(self, h, typ):
+        return self._clock(self.lib.nvmlDeviceGetClockInfo, h, typ)
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h):
+        v = self.ct.c_ulonglong()
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self._chk(fn(h, self.ct.byref(v)))
+        return v.value
+
+
 class ClockSampler:
     """Samples the SM clock and clock-event (throttle) reasons of one GPU while
-    the timed region runs: NVML every 5 ms, plus one sample at entry and one
+    the timed region runs: NVML every 2 ms (the pynvml module, else the
+    driver's NVML library through ctypes), plus one sample at entry and one
     at exit; if NVML is unavailable, nvidia-smi queries instead."""
 
     REASONS = {
@@ -132,7 +192,7 @@ class ClockSampler:
         "hw_power_brake_slowdown": 0x80,
     }
 
-    def __init__(self, device, period_s: float = 0.005):
+    def __init__(self, device, period_s: float = 0.002):
         self.period = period_s
         self.samples, self.reasons = [], set()
         self.max_mhz = None
@@ -142,8 +202,11 @@ class ClockSampler:
         self.mode = None
         self.smi_index = str(device.index)
         try:
-            import pynvml
-            pynvml.nvmlInit()
+            try:
+                import pynvml
+                pynvml.nvmlInit()
+            except ImportError:
+                pynvml = _NvmlCtypes()
             self.nv = pynvml
             self.h = None
             try:
@@ -157,7 +220,7 @@ class ClockSampler:
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
             self._reasons_fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
                 getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
-            self.mode = "nvml"
+            self.mode = "nvml" if not isinstance(pynvml, _NvmlCtypes) else "nvml-ctypes"
         except Exception as e:  # fall back to nvidia-smi
             self.error = f"nvml: {type(e).__name__}: {e}"
             self.mode = "smi"
@@ -186,12 +249,12 @@ class ClockSampler:
 
     def sample(self):
         try:
-            (self._sample_nvml if self.mode == "nvml" else self._sample_smi)()
+            (self._sample_smi if self.mode == "smi" else self._sample_nvml)()
         except Exception as e:
             self.error = f"{self.mode}: {type(e).__name__}: {e}"
 
     def _run(self):
-        while not self._stop.wait(self.period if self.mode == "nvml" else 0.05):
+        while not self._stop.wait(0.05 if self.mode == "smi" else self.period):
             self.sample()
 
     def __enter__(self):
@@ -360,11 +423,13 @@ def step_groups(c):
                               lse=d["lse"], workspace=d["ws"], scale=scale)
             groups.append(("decode", dec))
     else:
-        def dec():
-            E.kv_cache_append(c["kcache"], c["vcache"], c["k_new"], c["v_new"], c["cache_len"])
-            E.attn_decode(c["q"], c["kcache"], c["vcache"], c["kv_len"], o=c["o"], lse=c["lse"],
-                          workspace=c["ws"], scale=scale)
-        groups.append(("decode", dec))
+        # the decode step: append the new token, then decode (split + combine);
+        # two groups so that the decode call has its own time
+        groups.append(("append", lambda: E.kv_cache_append(
+            c["kcache"], c["vcache"], c["k_new"], c["v_new"], c["cache_len"])))
+        groups.append(("decode", lambda: E.attn_decode(
+            c["q"], c["kcache"], c["vcache"], c["kv_len"], o=c["o"], lse=c["lse"],
+            workspace=c["ws"], scale=scale)))
     return groups
 
 
@@ -433,12 +498,14 @@ def time_graphs(E, c, steps, flush, clk=None, sync=None):
 
 def other_workloads(E, skip, device, steps, peaks):
     """The other benchmark workloads, timed the same way (one entry each):
-    the compute-bound prefills and the HBM-bound decode behind the metric."""
+    the short and padded prefills (and the long-context one when it is not
+    the headline), the decode step (when it has no block of its own), the
+    backward passes and the E4M3 prefills."""
     import torch
     out = {}
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    for wid in (3, 4, 5):
-        if wid == skip:
+    for wid in (2, 3, 5, 4):
+        if wid in skip:
             continue
         c = build_case(wid, device)
         w = c["w"]
@@ -448,15 +515,22 @@ def other_workloads(E, skip, device, steps, peaks):
         torch.cuda.synchronize()
         _, kern_ms, _ = time_graphs(E, c, steps, flush)
         if w.kind == "prefill":
-            v = c["flops"] / (kern_ms["prefill"] * 1e-3) / 1e12
+            kl = None if c["key_lens"] is None else c["key_lens"].cpu().numpy()
+            v = prefill_flops(w, kl) / (kern_ms["prefill"] * 1e-3) / 1e12
             out[str(wid)] = {"workload": w.name, "value": v, "unit": "TFLOPS",
                              "ms": kern_ms["prefill"], "kernel": "fwd_bf16_tc_kernel",
                              "frac": v / peaks["bf16_tflops"],
                              "traffic": profiled_traffic(wid)}
+            if "dec" in c:
+                gbs = c["dec_bytes"] / (kern_ms["decode"] * 1e-3) / 1e9
+                out[str(wid)]["next_token_decode"] = {
+                    "value": gbs, "unit": "GB/s", "ms": kern_ms["decode"],
+                    "kernels": "kv_append_kernel, decode_split_mma_kernel, decode_combine_kernel",
+                    "frac": gbs / peaks["hbm_gbs"]}
         else:
             v = c["dec_bytes"] / (kern_ms["decode"] * 1e-3) / 1e9
             out[str(wid)] = {"workload": w.name, "value": v, "unit": "GB/s",
-                             "ms": kern_ms["decode"],
+                             "ms": kern_ms["decode"], "append_ms": kern_ms["append"],
                              "kernel": "decode_split_mma_kernel+decode_combine_kernel",
                              "frac": v / peaks["hbm_gbs"], "traffic": profiled_traffic(wid)}
         del c
@@ -581,79 +655,66 @@ def backward_workloads(E, device, steps, peaks, flush):
     return out
 
 
+def e2e_buffers(c):
+    """(device inputs {name: tensor}, device results [tensor]) of one step as
+    a user of the public API sees it: what is copied in from the host before
+    the calls and read back after them."""
+    w = c["w"]
+    if "bwd" in c:
+        # backward: inputs q, k, v, dO, O, LSE; results dQ, dK, dV
+        bw = c["bwd"]
+        return ({"q": c["q"], "k": c["k"], "v": c["v"], "do": bw["do"], "o": bw["o"],
+                 "lse": bw["lse"]}, [bw[n] for n in ("dq", "dk", "dv")])
+    if "fp8" in c:
+        # E4M3 prefill: inputs the quantised q, k, v; results O, LSE
+        f = c["fp8"]
+        return {n: f[n] for n in ("q", "k", "v")}, [c["o"], c["lse"]]
+    if w.kind == "prefill":
+        dev_in = {n: c[n] for n in ("q", "k", "v")}
+        dev_out = [c["o"], c["lse"]]
+        if "dec" in c:
+            d = c["dec"]
+            dev_in.update({"dec_" + n: d[n] for n in ("q", "k_new", "v_new")})
+            dev_out += [d["o"], d["lse"]]
+        return dev_in, dev_out
+    # decode step: the new token's q, k, v in; O and LSE out (the cache stays
+    # resident on the device between steps, as in generation)
+    return {n: c[n] for n in ("q", "k_new", "v_new")}, [c["o"], c["lse"]]
+
+
 def run_e2e(E, c, steps, device):
     """Same step through the public API with pinned host buffers: H2D copy of
-    the step's inputs, the step, D2H copy of its outputs, all timed."""
+    the step's inputs, the library calls, D2H copy of its results, all timed
+    on the stream with CUDA events between the three phases.  Returns a dict
+    with the mean ms per step, the mean ms of each phase and the bytes."""
     import torch
-    w = c["w"]
-    if "bwd" in c or "fp8" in c:
-        if "bwd" in c:
-            # backward: inputs q, k, v, dO, O, LSE; results dQ, dK, dV
-            bw = c["bwd"]
-            dev_in = {"q": c["q"], "k": c["k"], "v": c["v"], "do": bw["do"], "o": bw["o"],
-                      "lse": bw["lse"]}
-            dev_out = [bw[n] for n in ("dq", "dk", "dv")]
-        else:
-            # E4M3 prefill: inputs the quantised q, k, v; results O, LSE
-            f = c["fp8"]
-            dev_in = {n: f[n] for n in ("q", "k", "v")}
-            dev_out = [c["o"], c["lse"]]
-        host_in = {n: t.cpu().pin_memory() for n, t in dev_in.items()}
-        outs = [(torch.empty(t.shape, dtype=t.dtype).pin_memory(), t) for t in dev_out]
-        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-        d2h = sum(h.numel() * h.element_size() for h, _ in outs)
-        s0 = torch.cuda.Event(enable_timing=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-        total = 0.0
-        for _ in range(steps):
-            flush.zero_()
-            s0.record()
-            for n, t in dev_in.items():
-                t.copy_(host_in[n], non_blocking=True)
-            run_step(E, c)
-            for h, dv in outs:
-                h.copy_(dv, non_blocking=True)
-            s1.record()
-            s1.synchronize()
-            total += s0.elapsed_time(s1)
-        return total / steps, h2d, d2h
-    names_in = ["q", "k", "v"] if w.kind == "prefill" else ["q", "k_new", "v_new"]
-    host_in = {n: c[n].cpu().pin_memory() for n in names_in}
-    host_o = torch.empty(c["o"].shape, dtype=c["o"].dtype).pin_memory()
-    host_l = torch.empty(c["lse"].shape, dtype=torch.float32).pin_memory()
+    dev_in, dev_out = e2e_buffers(c)
+    host_in = {n: t.cpu().pin_memory() for n, t in dev_in.items()}
+    outs = [(torch.empty(t.shape, dtype=t.dtype).pin_memory(), t) for t in dev_out]
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = host_o.numel() * host_o.element_size() + host_l.numel() * 4
-    extra_out = []
-    if "dec" in c:
-        d = c["dec"]
-        for n in ("q", "k_new", "v_new"):
-            host_in["dec_" + n] = d[n].cpu().pin_memory()
-            h2d += d[n].numel() * d[n].element_size()
-        extra_out = [(torch.empty(d["o"].shape, dtype=d["o"].dtype).pin_memory(), d["o"]),
-                     (torch.empty(d["lse"].shape, dtype=torch.float32).pin_memory(), d["lse"])]
-        d2h += sum(h.numel() * h.element_size() for h, _ in extra_out)
-    s0 = torch.cuda.Event(enable_timing=True)
-    s1 = torch.cuda.Event(enable_timing=True)
+    d2h = sum(h.numel() * h.element_size() for h, _ in outs)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    total = 0.0
-    for _ in range(steps):
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+    for s in range(steps):
         flush.zero_()
-        s0.record()
-        for n in names_in:
-            c[n].copy_(host_in[n], non_blocking=True)
-        if "dec" in c:
-            for n in ("q", "k_new", "v_new"):
-                c["dec"][n].copy_(host_in["dec_" + n], non_blocking=True)
+        ev[s][0].record()
+        for n, t in dev_in.items():
+            t.copy_(host_in[n], non_blocking=True)
+        ev[s][1].record()
         run_step(E, c)
-        host_o.copy_(c["o"], non_blocking=True)
-        host_l.copy_(c["lse"], non_blocking=True)
-        for h, dv in extra_out:
+        ev[s][2].record()
+        for h, dv in outs:
             h.copy_(dv, non_blocking=True)
-        s1.record()
-        s1.synchronize()
-        total += s0.elapsed_time(s1)
-    return total / steps, h2d, d2h
+        ev[s][3].record()
+        ev[s][3].synchronize()            # the results are on the host
+
+    def mean(a, b):
+        return sum(e[a].elapsed_time(e[b]) for e in ev) / steps
+    return {"ms": mean(0, 3), "h2d_ms": mean(0, 1), "call_ms": mean(1, 2),
+            "d2h_ms": mean(2, 3), "h2d": h2d, "d2h": d2h}
+
+
+_CPU_INPUTS = {}
 
 
 def cpu_baseline(wid, budget_s=12.0, seed=0):
@@ -667,16 +728,19 @@ def cpu_baseline(wid, budget_s=12.0, seed=0):
     cores = oracle.default_threads()
     rng = np.random.default_rng(seed)
     if w.kind == "prefill":
-        if wid in (2,):
-            x = workloads.workload_inputs(wid, device="cpu")
-        else:  # same shapes; a smaller batch keeps host memory modest
-            x = workloads.prefill_inputs(1, w.Hq, w.Hkv, w.T, w.S, w.D, w.dtype, seed=wid,
-                                         q_scale=w.q_scale)
-        arr = [workloads.to_numpy_exact(x[n])[0] for n in ("q", "k", "v")]
+        if wid not in _CPU_INPUTS:   # drawn once per process (the reference arm calls again)
+            if wid in (2,):
+                x = workloads.workload_inputs(wid, device="cpu")
+            else:  # same shapes; a smaller batch keeps host memory modest
+                x = workloads.prefill_inputs(1, w.Hq, w.Hkv, w.T, w.S, w.D, w.dtype, seed=wid,
+                                             q_scale=w.q_scale)
+            arr = [workloads.to_numpy_exact(x[n])[0] for n in ("q", "k", "v")]
+            lens = x["key_lens"].numpy() if x["key_lens"] is not None else None
+            if lens is None and w.lens is not None:
+                lens = workloads.lengths(wid, w.lens[0], w.lens[1], arr[0].shape[0])
+            _CPU_INPUTS[wid] = (arr, lens)
+        arr, lens = _CPU_INPUTS[wid]
         Bx = arr[0].shape[0]
-        lens = x["key_lens"].numpy() if x["key_lens"] is not None else None
-        if lens is None and w.lens is not None:
-            lens = workloads.lengths(wid, w.lens[0], w.lens[1], Bx)
         n_rows_total = Bx * w.Hq * w.T
         done_flops, t_used, rows_done = 0.0, 0.0, 0
         chunk = 256
@@ -698,9 +762,11 @@ def cpu_baseline(wid, budget_s=12.0, seed=0):
             chunk = min(chunk * 2, 8192)
         return done_flops / t_used / 1e12, "TFLOPS", cores, \
             f"{rows_done} random query rows of {w.name} (visible-key FLOPs), {t_used:.1f} s"
-    d = workloads.decode_inputs(8, w.Hq, w.Hkv, w.D, w.lens[0], w.lens[1], w.dtype, seed=wid)
-    arr = [workloads.to_numpy_exact(d[n])[0] for n in ("q", "kcache", "vcache")]
-    kv = d["kv_len"].numpy()
+    if wid not in _CPU_INPUTS:
+        d = workloads.decode_inputs(8, w.Hq, w.Hkv, w.D, w.lens[0], w.lens[1], w.dtype, seed=wid)
+        _CPU_INPUTS[wid] = ([workloads.to_numpy_exact(d[n])[0] for n in ("q", "kcache", "vcache")],
+                            d["kv_len"].numpy())
+    arr, kv = _CPU_INPUTS[wid]
     t_used, nbytes, reps = 0.0, 0.0, 0
     while t_used < budget_s:
         t0 = time.perf_counter()
@@ -753,6 +819,114 @@ def cpu_baseline_bwd(wid, budget_s=12.0, seed=0):
 
 # ------------------------------------------------------------------- arms
 
+def measure_block(E, args, wid, device, peaks, ws, rank, backward=False, fp8=False,
+                  batch=None):
+    """One workload measured for the JSON line: warm-up steps, K timed steps
+    (CUDA-graph replays, L2 flushed between steps, clocks sampled, barrier and
+    max over ranks), the roofline of its dominant kernel, the end-to-end
+    figure through the public API, and (rank 0) the float64 oracle timed on
+    the host cores.  Returns the block's dict."""
+    import torch
+    c = build_case(wid, device, batch, backward=backward, fp8=fp8)
+    w = c["w"]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    for _ in range(args.warmup):
+        flush.zero_()
+        run_step(E, c)
+    torch.cuda.synchronize()
+    if E.attn_device_error(clear=True) != 0:
+        raise RuntimeError("device error during warm-up")
+
+    K = args.steps
+    clk = ClockSampler(device)
+    step_ms, kern_ms, launches_per_step = time_graphs(E, c, K, flush, clk,
+                                                      sync=lambda: barrier(ws))
+    total_ms = reduce_max(sum(step_ms), ws, device)
+    if E.attn_device_error(clear=True) != 0:
+        raise RuntimeError("device error during the timed region")
+    ms_per_step = total_ms / K
+    out = {"value": None, "unit": None, "ms_per_step": ms_per_step, "dtype": "bf16"}
+    if w.kind == "prefill":
+        out["value"] = c["flops"] * ws / (ms_per_step * 1e-3) / 1e12
+        out["unit"] = "TFLOPS"
+        kl = None if c["key_lens"] is None else c["key_lens"].cpu().numpy()
+        achieved = (c["flops"] if "bwd" in c else prefill_flops(w, kl)) \
+            / (kern_ms["prefill"] * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        kernel = ("bwd_delta_kernel+bwd_dq_kernel+bwd_dkdv_kernel" if "bwd" in c else
+                  "fwd_bf16_tc_kernel<128,0,1>" if "fp8" in c else
+                  f"fwd_bf16_tc_kernel<{w.D},0,0>")
+        peak_source = peaks["source"] + " bf16 burst (kernel timed alone)"
+        if "fp8" in c:
+            # a contraction takes the peak of its own type: the measured bf16
+            # burst times the nominal FP8 / bf16 ratio (4.5 / 2.25 PFLOP/s)
+            peak *= 2.0
+            peak_source += " x 2 (nominal FP8/bf16 ratio)"
+            out["dtype"] = "e4m3"
+        traffic = profiled_traffic(wid) if batch is None and not backward and not fp8 else None
+        out["roofline"] = {"kernel": kernel, "bound": "tensor",
+                           "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                           "frac": achieved / peak, "traffic": traffic,
+                           "peak_source": peak_source, "kernel_ms": kern_ms["prefill"]}
+        if "dec" in c:
+            gbs = c["dec_bytes"] / (kern_ms["decode"] * 1e-3) / 1e9
+            out["next_token_decode"] = {
+                "workload": "next-token append + decode of the same batch (kv_len 1025)",
+                "ms": kern_ms["decode"], "value": gbs, "unit": "GB/s",
+                "frac": gbs / peaks["hbm_gbs"]}
+    else:
+        out["value"] = c["dec_bytes"] * ws / (ms_per_step * 1e-3) / 1e9
+        out["unit"] = "GB/s"
+        achieved = c["dec_bytes"] / (kern_ms["decode"] * 1e-3) / 1e9
+        out["roofline"] = {"kernel": "decode_split_mma_kernel+decode_combine_kernel",
+                           "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                           "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                           "traffic": profiled_traffic(wid) if batch is None else None,
+                           "peak_source": peaks["source"] + " HBM copy",
+                           "kernel_ms": kern_ms["decode"], "append_ms": kern_ms["append"]}
+    cfg = {"workload": ("backward (dQ, dK, dV, 2.5x the forward's FLOPs) of: " + w.name
+                        if "bwd" in c else
+                        "E4M3 inputs (per-tensor descales): " + w.name if "fp8" in c else w.name),
+           "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+           "l2": "flushed between steps (256 MiB write, outside the timed events)",
+           "timing": "CUDA events around CUDA-graph replays of each kernel group of the step",
+           "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+           "algorithmic_work_per_step": c["flops"] if w.kind == "prefill" else c["dec_bytes"]}
+    if w.kind == "prefill":
+        cfg.update({"T": w.T, "S": w.S, "causal": w.causal,
+                    "key_lens": None if w.lens is None else f"U[{w.lens[0]},{w.lens[1]}]"})
+        if w.q_scale != 1.0:
+            cfg["q_scale"] = w.q_scale
+    else:
+        cfg.update({"cache_len": f"U[{w.lens[0]},{w.lens[1]}]", "S_max": c["S_max"],
+                    "kv_bytes_per_step": c["dec_bytes"]})
+    out["config"] = cfg
+    out["gpu_launches"] = int(launches_per_step * K)
+    out["clocks"] = clk.record()
+
+    if not args.no_e2e:
+        # End to end through the public API with host buffers.
+        e = run_e2e(E, c, max(3, min(K, 20)), device)
+        e2e_ms = reduce_max(e["ms"], ws, device)
+        work = c["flops"] if w.kind == "prefill" else c["dec_bytes"]
+        scale = 1e12 if w.kind == "prefill" else 1e9
+        out["e2e"] = {"value": work * ws / (e2e_ms * 1e-3) / scale, "unit": out["unit"],
+                      "ms_per_step": e2e_ms, "h2d_bytes_per_step": int(e["h2d"]),
+                      "d2h_bytes_per_step": int(e["d2h"]),
+                      "breakdown_ms": {"h2d_copies": e["h2d_ms"], "library_calls": e["call_ms"],
+                                       "d2h_copies": e["d2h_ms"]},
+                      "copy_gbs": (e["h2d"] + e["d2h"]) / ((e["h2d_ms"] + e["d2h_ms"]) * 1e-3)
+                      / 1e9}
+    del c
+    torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        fn = cpu_baseline_bwd if backward else cpu_baseline
+        v, unit, cores, sample = fn(wid, budget_s=args.cpu_budget)
+        out["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
+                               "sample": sample}
+    return out
+
+
 def bench_ours(args):
     import torch
     ws, rank, local = dist_env()
@@ -773,109 +947,27 @@ def bench_ours(args):
         raise SystemExit("--backward and --fp8 need a prefill workload (2, 3 or 5)")
     if args.backward and args.fp8:
         raise SystemExit("--backward and --fp8 are separate modes")
-    c = build_case(args.workload, device, args.batch, backward=args.backward, fp8=args.fp8)
-    w = c["w"]
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-    for _ in range(args.warmup):
-        flush.zero_()
-        run_step(E, c)
-    torch.cuda.synchronize()
-    if E.attn_device_error(clear=True) != 0:
-        raise RuntimeError("device error during warm-up")
 
-    K = args.steps
-    clk = ClockSampler(device)
-    step_ms, kern_ms, launches_per_step = time_graphs(E, c, K, flush, clk,
-                                                      sync=lambda: barrier(ws))
-    launches = launches_per_step * K
-    total_ms = reduce_max(sum(step_ms), ws, device)
-    if E.attn_device_error(clear=True) != 0:
-        raise RuntimeError("device error during the timed region")
-
-    ms_per_step = total_ms / K
-    total_flops = c["flops"] * ws
+    head = measure_block(E, args, args.workload, device, peaks, ws, rank,
+                         backward=args.backward, fp8=args.fp8, batch=args.batch)
     out = {
         "metric": METRIC,
-        "value": None, "unit": None,
-        "n_gpus": ws, "steps": K, "warmup": args.warmup,
-        "ms_per_step": ms_per_step,
+        "value": head.pop("value"), "unit": head.pop("unit"),
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": head.pop("ms_per_step"),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic",
+        "dtype": head.pop("dtype"), "data": "synthetic",
     }
-    if w.kind == "prefill":
-        out["value"] = total_flops / (ms_per_step * 1e-3) / 1e12
-        out["unit"] = "TFLOPS"
-        achieved = (c["flops"] if "bwd" in c else
-                    prefill_flops(w, None if c["key_lens"] is None else c["key_lens"].cpu().numpy())
-                    ) / (kern_ms["prefill"] * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
-        kernel = ("bwd_delta_kernel+bwd_dq_kernel+bwd_dkdv_kernel" if "bwd" in c else
-                  "fwd_bf16_tc_kernel<128,0,1>" if "fp8" in c else "fwd_bf16_tc_kernel")
-        peak_source = peaks["source"] + " bf16 burst"
-        if "fp8" in c:
-            # a contraction takes the peak of its own type: the measured bf16
-            # burst times the nominal FP8 / bf16 ratio (4.5 / 2.25 PFLOP/s)
-            peak *= 2.0
-            peak_source += " x 2 (nominal FP8/bf16 ratio)"
-            out["dtype"] = "e4m3"
-        traffic = (profiled_traffic(args.workload)
-                   if args.batch is None and not args.backward and not args.fp8 else None)
-        out["roofline"] = {"kernel": kernel, "bound": "tensor",
-                           "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                           "frac": achieved / peak, "traffic": traffic,
-                           "peak_source": peak_source}
-        if "dec" in c:
-            gbs = c["dec_bytes"] / (kern_ms["decode"] * 1e-3) / 1e9
-            out["decode"] = {"workload": "next-token decode of the same batch (kv_len 1025)",
-                             "ms": kern_ms["decode"], "value": gbs, "unit": "GB/s",
-                             "frac": gbs / peaks["hbm_gbs"]}
-        out["prefill_ms"] = kern_ms["prefill"]
-    else:
-        gbs_job = c["dec_bytes"] * ws / (ms_per_step * 1e-3) / 1e9
-        out["value"] = gbs_job
-        out["unit"] = "GB/s"
-        achieved = c["dec_bytes"] / (kern_ms["decode"] * 1e-3) / 1e9
-        out["roofline"] = {"kernel": "decode_split_kernel+decode_combine_kernel",
-                           "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                           "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                           "traffic": profiled_traffic(args.workload) if args.batch is None else None,
-                           "peak_source": peaks["source"] + " HBM copy"}
-    cfg = {"workload": ("backward (dQ, dK, dV, 2.5x the forward's FLOPs) of: " + w.name
-                        if "bwd" in c else
-                        "E4M3 inputs (per-tensor descales): " + w.name if "fp8" in c else w.name),
-           "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
-           "l2": "flushed between steps (256 MiB write, outside the timed events)",
-           "timing": "CUDA events around CUDA-graph replays of each kernel group of the step",
-           "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-           "algorithmic_work_per_step": c["flops"] if w.kind == "prefill" else c["dec_bytes"]}
-    if w.kind == "prefill":
-        cfg.update({"T": w.T, "S": w.S, "causal": w.causal,
-                    "key_lens": None if w.lens is None else f"U[{w.lens[0]},{w.lens[1]}]"})
-    else:
-        cfg.update({"cache_len": f"U[{w.lens[0]},{w.lens[1]}]", "S_max": c["S_max"]})
-    out["config"] = cfg
-    out["gpu_launches"] = int(launches)
-    out["clocks"] = clk.record()
-
-    # End to end through the public API with host buffers.
-    e2e_ms, h2d, d2h = run_e2e(E, c, max(3, min(K, 20)), device)
-    e2e_ms = reduce_max(e2e_ms, ws, device)
-    if w.kind == "prefill":
-        e2e_val = c["flops"] * ws / (e2e_ms * 1e-3) / 1e12
-    else:
-        e2e_val = c["dec_bytes"] * ws / (e2e_ms * 1e-3) / 1e9
-    out["e2e"] = {"value": e2e_val, "unit": out["unit"], "ms_per_step": e2e_ms,
-                  "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
-
+    out.update(head)
+    plain = not args.backward and not args.fp8 and args.batch is None
+    skip = {args.workload}
+    if plain and workloads_kind(args.workload) == "prefill" and not args.no_decode_block:
+        # the metric's other half: the GQA decode step, with its own block
+        out["decode"] = measure_block(E, args, 4, device, peaks, ws, rank)
+        skip.add(4)
     if not args.no_other_workloads and args.batch is None:
-        out["other_workloads"] = other_workloads(E, args.workload, device,
-                                                 max(3, min(K, 10)), peaks)
-
-    if rank == 0 and not args.no_cpu_baseline:
-        fn = cpu_baseline_bwd if args.backward else cpu_baseline
-        v, unit, cores, sample = fn(args.workload, budget_s=args.cpu_budget)
-        out["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
-                               "sample": sample}
+        out["other_workloads"] = other_workloads(E, skip, device, max(3, min(args.steps, 10)),
+                                                 peaks)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if ws > 1:
@@ -904,8 +996,10 @@ def bench_reference(args):
            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": wall / args.steps * 1e3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
-                      "parallelism": "host cores"},
+           "config": dict({"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "D": w.D,
+                           "parallelism": "host cores"},
+                          **({"T": w.T, "S": w.S, "causal": w.causal} if w.kind == "prefill"
+                             else {"cache_len": f"U[{w.lens[0]},{w.lens[1]}]"})),
            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
                             "sample": samples[0] + f" (per step; {args.steps} steps)"},
            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0,
@@ -916,9 +1010,9 @@ def bench_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5])
+    ap.add_argument("--workload", type=int, default=3, choices=[2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -928,6 +1022,10 @@ def main(argv=None):
                     help="time the prefill workload on E4M3 inputs (attn_fwd_fp8) instead")
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip timing the other benchmark workloads")
+    ap.add_argument("--no-decode-block", action="store_true",
+                    help="skip the decode block that follows a prefill headline")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end (host buffer) measurement")
     ap.add_argument("--batch", type=int, default=None,
                     help="smaller batch of the same workload (ncu profiling cases only)")
     args = ap.parse_args(argv)

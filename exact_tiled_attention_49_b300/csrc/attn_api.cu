@@ -492,9 +492,16 @@ size_t attn_decode_workspace_size(int B, int Hq, int S_max, int D) {
   return (size_t)B * Hq * attn::decode::max_splits(S_max) * ((size_t)D + 2) * sizeof(float);
 }
 
-int attn_decode(const void* q, const void* kcache, const void* vcache, const int32_t* kv_lens,
-                void* o, float* lse, int B, int Hq, int Hkv, int S_max, int D, int dtype,
-                float scale, void* workspace, size_t ws_bytes, attn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Argument and shape checks of a decode step (everything but the workspace),
+// shared by attn_decode and attn_decode_noalloc so that both report the same
+// status for the same request.
+int decode_validate(const void* q, const void* kcache, const void* vcache,
+                    const int32_t* kv_lens, const void* o, const float* lse, int B, int Hq,
+                    int Hkv, int S_max, int D, int dtype, float scale) {
   if (!q || !kcache || !vcache || !kv_lens || !o) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || S_max <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0 || !finite_positive(scale)) return ATTN_ERR_INVALID_ARG;
@@ -506,6 +513,20 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, const int
   if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o) ||
       !aligned4(kv_lens) || (lse != nullptr && !aligned4(lse)))
     return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_decode(const void* q, const void* kcache, const void* vcache, const int32_t* kv_lens,
+                void* o, float* lse, int B, int Hq, int Hkv, int S_max, int D, int dtype,
+                float scale, void* workspace, size_t ws_bytes, attn_stream_t stream) {
+  const int rc = decode_validate(q, kcache, vcache, kv_lens, o, lse, B, Hq, Hkv, S_max, D, dtype,
+                                 scale);
+  if (rc != ATTN_OK) return rc;
+  const int G = Hq / Hkv;
   const size_t need = attn_decode_workspace_size(B, Hq, S_max, D);
   if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
 
@@ -574,8 +595,12 @@ extern "C" {
 int attn_decode_noalloc(const void* q, const void* kcache, const void* vcache,
                         const int32_t* kv_lens, void* o, float* lse, int B, int Hq, int Hkv,
                         int S_max, int D, int dtype, float scale, attn_stream_t stream) {
+  // The same checks as attn_decode first, so that an invalid or unsupported
+  // request is reported as such rather than as too large for the scratch.
+  const int rc = decode_validate(q, kcache, vcache, kv_lens, o, lse, B, Hq, Hkv, S_max, D, dtype,
+                                 scale);
+  if (rc != ATTN_OK) return rc;
   const size_t need = attn_decode_workspace_size(B, Hq, S_max, D);
-  if (need == 0) return ATTN_ERR_INVALID_ARG;
   if (need > ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_WORKSPACE;
   void* scratch = noalloc_scratch();
   if (scratch == nullptr) return ATTN_ERR_CUDA;

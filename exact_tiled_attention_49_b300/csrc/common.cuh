@@ -363,8 +363,6 @@ __device__ __forceinline__ void st_shared_zero16(uint32_t addr) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0) : "memory");
 }
 
-// Make this thread's generic-proxy shared-memory writes visible to the async
-// proxy (TMA, tcgen05.mma operand reads).
 // Division of 0 <= n < 2^31 by an invariant d >= 1 with one multiply-high
 // and no divide sequence (whose reciprocal step would queue behind the
 // softmax's exponentials on the same pipe).  Granlund and Montgomery,
@@ -385,6 +383,8 @@ __device__ __forceinline__ int fast_div(int n, FastDiv f) {
   return (int)((__umulhi((uint32_t)n, f.m) + (uint32_t)n) >> f.s);
 }
 
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (TMA, tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -407,7 +407,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Two floats -> packed fp16x2 (round to nearest even); `lo` in bits 0-15.
 // Four floats to E4M3 (round to nearest even, saturating to +-448), packed
 // in K order: byte 0 holds `a`.  The conversion writes its first source to
 // the upper byte of each pair.
@@ -417,6 +416,7 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(d), "f"(c));
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
+// Two floats -> packed fp16x2 (round to nearest even); `lo` in bits 0-15.
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

@@ -388,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tm_v);
     }
     int ring = 0, qi = 0, ntail = 0;
+    int nq0 = 0, nq1 = 0;  // phases armed so far on q_full[0] and q_full[1]
     bool ok = true;
     auto wait_bar = [&](uint32_t bar, uint32_t parity) {
       const bool w = mbar_wait(bar, parity, 1, abort_flag);
@@ -407,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Query tile t of the item with row x.q0 into its buffer (qi-th use).
     auto load_q = [&](const Item& x, int t) {
       if (qi > 0 && !(ok = wait_bar(bar_qempty(t), (qi - 1) & 1))) return;
+      ++(t ? nq1 : nq0);
       if (lane == 0) {
         if (x.q0 + t * kBM < 0) {
           mbar_arrive(bar_qfull(t));  // virtual tile: nothing to load
@@ -484,11 +486,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       early = early_next;
     }
     // Drain: every issued copy must land before the CTA may exit (the last
-    // kSlots ring entries cover every slot's latest copy).
+    // kSlots ring entries cover every slot's latest copy).  Each Q buffer's
+    // latest armed phase is waited for, which includes a next item's Q_0
+    // issued early by a loop that then gave up on that item's K_0.
     for (int u = max(0, ring - C::kSlots); u < ring; ++u)
       mbar_wait(bar_full(u % C::kSlots), (u / C::kSlots) & 1, 3);
-    if (qi > 0)
-      for (int t = 0; t < kQTiles; ++t) mbar_wait(bar_qfull(t), (qi - 1) & 1, 3);
+    if (nq0 > 0) mbar_wait(bar_qfull(0), (nq0 - 1) & 1, 3);
+    if (nq1 > 0) mbar_wait(bar_qfull(1), (nq1 - 1) & 1, 3);
     if (ntail > 0) mbar_wait(bar_tail, (ntail - 1) & 1, 3);
     __syncwarp();
   } else if (warp == kMmaWarp) {

@@ -163,9 +163,14 @@ ATTN_API int attn_fwd_chunked(const void* q, const void* kcache, const void* vca
                               int causal, float scale, attn_stream_t stream);
 
 /*
- * attn_bwd_workspace_size -- bytes of device scratch attn_bwd needs (one
- * float per query row: delta = rowsum(dO * O)).  Returns 0 for invalid
- * sizes.
+ * attn_bwd_workspace_size -- bytes of device scratch attn_bwd needs: one
+ * float per query row for delta = rowsum(dO * O), the row term of the
+ * softmax's chain rule that the backward forms once and reads for every key
+ * tile ("Hands-on build guide: FlashAttention-style tiled attention kernel
+ * in pure NumPy", Roadmap: gradient through attention by the chain rule;
+ * "Self-Attention: Implementation, Complexity, and Efficient Variants",
+ * FlashAttention: O(n) memory, nothing of size T x S is stored).  Returns 0
+ * for invalid sizes.
  */
 ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int T);
 
@@ -214,8 +219,14 @@ ATTN_API int attn_bwd(const void* q, const void* k, const void* v, const void* o
 /*
  * attn_decode_workspace_size -- bytes of device scratch attn_decode needs for
  * a batch of B sequences, Hq query heads, caches of S_max positions and head
- * size D.  The caller allocates it (any alignment >= 16 bytes) and may reuse
- * it across calls on the same stream.  Returns 0 for invalid sizes.
+ * size D: the partial results (unnormalised output, running maximum and
+ * denominator) of the pieces of the cache that are reduced independently
+ * before they are merged with the online softmax's rescaling ("Implementing
+ * attention from scratch", Core ideas, Stable softmax: partial sums kept
+ * against a running maximum and rescaled by exp(m_old - m_new); KV caching:
+ * one decode step reads the whole cache).  The caller allocates it (any
+ * alignment >= 16 bytes) and may reuse it across calls on the same stream.
+ * Returns 0 for invalid sizes.
  */
 ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int S_max, int D);
 

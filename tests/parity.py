@@ -81,3 +81,40 @@ def compare(o_gpu: torch.Tensor, lse_gpu, o_ref: np.ndarray, lse_ref: np.ndarray
             assert stats["lse_max"] <= tol["lse"], \
                 f"{what}: LSE max abs err {stats['lse_max']:.3g} > {tol['lse']}"
     return stats
+
+
+def sample_rows(B, Hq, T, S, lens, per_head, seed, q_off=None):
+    """Flat row ids (b*Hq + h)*T + i to compare one by one: the first and
+    last rows of each head, the rows around the first two tile boundaries,
+    the rows at and after each sequence's valid length, and `per_head`
+    seeded random rows per head."""
+    rng = np.random.default_rng(seed)
+    rows = []
+    off = S - T if q_off is None else q_off
+    for b in range(B):
+        L = S if lens is None else int(lens[b])
+        for h in range(Hq):
+            base = (b * Hq + h) * T
+            pick = {0, 1, 127, 128, 255, 256, T - 2, T - 1, max(L - off - 1, 0),
+                    min(max(L - off, 0), T - 1)}
+            pick |= set(rng.integers(0, T, size=per_head).tolist())
+            rows.extend(base + i for i in sorted(pick) if 0 <= i < T)
+    return np.array(rows, dtype=np.int64)
+
+
+def gather_rows(o: torch.Tensor, lse: torch.Tensor, rows: np.ndarray, D: int):
+    """The GPU outputs of the given flat rows: (o [n, D], lse [n])."""
+    idx = torch.from_numpy(rows).to(o.device)
+    return o.reshape(-1, D).index_select(0, idx), lse.reshape(-1).index_select(0, idx)
+
+
+def assert_padded_rows_zero(o: torch.Tensor, lse: torch.Tensor, lens, S: int):
+    """Every padded query row (position >= L_b, bottom-right alignment) is
+    exactly 0 with LSE = -inf, and every other row has a finite LSE."""
+    B, Hq, T, _ = o.shape
+    for b in range(B):
+        L = int(lens[b])
+        first_pad = max(0, min(T, L - (S - T)))
+        assert torch.all(o[b, :, first_pad:] == 0), f"padded rows of sequence {b} not zero"
+        assert torch.all(torch.isneginf(lse[b, :, first_pad:]))
+        assert torch.all(torch.isfinite(lse[b, :, :first_pad]))

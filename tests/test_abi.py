@@ -108,6 +108,27 @@ def test_decode_rejects_bad_arguments(lib):
     assert dec(ws_bytes=ws - 4) == 3
 
 
+def test_decode_noalloc_checks_arguments_before_its_scratch(lib):
+    """attn_decode_noalloc reports an invalid or unsupported request the way
+    attn_decode does, even when its workspace would exceed the fixed
+    scratch array (which alone would give ATTN_ERR_WORKSPACE)."""
+    big = (64, 32, 8, 100000)            # B, Hq, Hkv, S_max: far beyond the scratch
+
+    def na(q=FAKE, D=128, Hq=32, Hkv=8, dt=1, scale=0.125):
+        B, _, _, S_max = big
+        return lib.attn_decode_noalloc(q, FAKE, FAKE, FAKE, FAKE, None, B, Hq, Hkv, S_max, D,
+                                       dt, scale, None)
+    from exact_tiled_attention_49_b300 import NOALLOC_SCRATCH_BYTES
+    assert lib.attn_decode_workspace_size(64, 32, 100000, 96) > NOALLOC_SCRATCH_BYTES
+    assert na(D=96) == 2                   # unsupported head size, not "too large"
+    assert na(q=None) == 1                 # invalid argument, not "too large"
+    assert na(Hq=6, Hkv=4) == 1
+    assert na(dt=7) == 1
+    assert na(scale=0.0) == 1
+    assert na(q=MIS) == 1
+    assert na() == 3                       # a valid request that does not fit
+
+
 def test_append_rejects_bad_arguments(lib):
     def app(D=64, dt=1, pos=FAKE, k=FAKE):
         return lib.kv_cache_append(k, FAKE, FAKE, FAKE, pos, 2, 2, 10, D, dt, None, None)
