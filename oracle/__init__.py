@@ -21,12 +21,13 @@ import os
 import numpy as np
 
 from .oracle_np import (attn_bwd_magnitudes_np, attn_bwd_np, attn_decode_np, attn_fwd_fp8_np,
-                        attn_fwd_np, attn_tiled_online_np, bf16_bits_to_f64, e4m3_bits_to_f64,
-                        visibility)
+                        attn_fwd_kv_shard_np, attn_fwd_np, attn_tiled_online_np,
+                        bf16_bits_to_f64, e4m3_bits_to_f64, lse_merge_np, visibility)
 
 __all__ = [
     "attn_fwd", "attn_decode", "kv_append", "attn_fwd_np", "attn_decode_np", "attn_bwd_np",
-    "attn_bwd_magnitudes_np", "attn_fwd_fp8_np", "e4m3_bits_to_f64",
+    "attn_bwd_magnitudes_np", "attn_fwd_fp8_np", "e4m3_bits_to_f64", "attn_fwd_kv_shard_np",
+    "lse_merge_np",
     "attn_tiled_online_np", "bf16_bits_to_f64", "visibility", "build",
     "default_threads",
 ]

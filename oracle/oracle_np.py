@@ -319,3 +319,70 @@ def attn_bwd_magnitudes_np(q, k, v, do, causal=False, key_lens=None, scale=None,
             ak[b, g] += scale * (ads.T @ np.abs(q[b, h]) + p.T @ (np.abs(q[b, h]) * rdo[:, None]))
             av[b, g] += p.T @ np.abs(do[b, h])
     return aq + np.abs(dq), ak + np.abs(dk), av + np.abs(dv)
+
+
+def attn_fwd_kv_shard_np(q, k, v, q_pos, key_lens, k_off, causal=True, scale=None, bf16=False):
+    """Attention of the queries over one shard of the keys, in float64.
+
+    "Building a causal self-attention block from scratch in PyTorch",
+    Extending It: distributed attention shards Q/K/V across devices and
+    recombines the results.  k, v [B,Hkv,S,D] hold the keys at global
+    positions k_off .. k_off + S - 1 of each sequence.  In global positions:
+    query row i of sequence b sits at q_pos[b] + i; key x is visible to it
+    iff x < key_lens[b] and (not causal, or x <= q_pos[b] + i); the row is
+    a padded row iff q_pos[b] + i >= key_lens[b].  The result is the
+    softmax over the visible keys of this shard only, with its LSE: (o
+    [B,Hq,T,D], lse [B,Hq,T]); rows that see no key of the shard (padded
+    rows included) are O = 0, LSE = -inf.
+    """
+    q, k, v = (_as_f64(x, bf16) for x in (q, k, v))
+    B, Hq, T, D = q.shape
+    _, Hkv, S, _ = k.shape
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    G = Hq // Hkv
+    o = np.zeros((B, Hq, T, D))
+    lse = np.full((B, Hq, T), _NEG_INF)
+    x = k_off + np.arange(S)                       # global key positions
+    for b in range(B):
+        L = int(key_lens[b])
+        pos = int(q_pos[b]) + np.arange(T)         # global query positions
+        vis = (x[None, :] < L) & (pos[:, None] < L)
+        if causal:
+            vis &= x[None, :] <= pos[:, None]
+        for h in range(Hq):
+            g = h // G
+            for i in range(T):
+                j = np.nonzero(vis[i])[0]
+                if j.size == 0:
+                    continue
+                s = scale * (k[b, g, j] @ q[b, h, i])
+                m = s.max()
+                e = np.exp(s - m)
+                o[b, h, i] = (e / e.sum()) @ v[b, g, j]
+                lse[b, h, i] = m + np.log(e.sum())
+    return o, lse
+
+
+def lse_merge_np(o_parts, lse_parts):
+    """Attention over the union of disjoint key sets from the partials over
+    each set, in float64: with Z_n = exp(LSE_n) the sum of exponentials of
+    part n and O_n its normalised output, the whole row has
+    Z = sum_n Z_n and O = sum_n Z_n O_n / Z ("Implementing attention from
+    scratch", Core ideas, Stable softmax: the same rescaling the online
+    softmax applies).  Computed against the largest LSE_n of the row; a row
+    with no finite LSE_n is O = 0, LSE = -inf.  o_parts [N,...,D],
+    lse_parts [N,...] -> (o [...,D], lse [...])."""
+    o_parts = np.asarray(o_parts, dtype=np.float64)
+    lse_parts = np.asarray(lse_parts, dtype=np.float64)
+    finite = np.isfinite(lse_parts)
+    m = np.where(finite, lse_parts, _NEG_INF).max(axis=0)
+    has = np.isfinite(m)
+    ref = np.where(has, m, 0.0)
+    w = np.where(finite, np.exp(np.where(finite, lse_parts, 0.0) - ref[None]), 0.0)
+    z = w.sum(axis=0)
+    zs = np.where(has, z, 1.0)
+    o = np.where(has[..., None], (w[..., None] * np.nan_to_num(o_parts)).sum(axis=0)
+                 / zs[..., None], 0.0)
+    lse = np.where(has, ref + np.log(zs), _NEG_INF)
+    return o, lse
