@@ -27,6 +27,9 @@ SIGNATURES = {
                               _P]),
     "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _F, _F, _F, _F,
                           _P]),
+    "attn_fwd_kv_shard": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                               _F, _P]),
+    "attn_lse_merge": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
     "attn_bwd_workspace_size": (ctypes.c_size_t, [_I, _I, _I]),
     "attn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _P,
                       _F, _P, ctypes.c_size_t, _P]),
@@ -231,6 +234,64 @@ def attn_fwd_chunked(q, kcache, vcache, q_pos, kv_lens, o=None, lse=None, causal
     rc = lib.attn_fwd_chunked(*ptrs, lp, qp, kl, B, Hq, Hkv, T, S_max, D, dt,
                               int(bool(causal)), float(scale), _stream(stream))
     _check(rc, "attn_fwd_chunked")
+    return o, lse
+
+
+def attn_fwd_kv_shard(q, k, v, q_pos, key_lens, k_off, o=None, lse=None, causal=True,
+                      scale=None, stream=None):
+    """Prefill over one shard of the keys.  q [B,Hq,T,D]; k/v [B,Hkv,S,D]
+    hold the keys at global positions k_off .. k_off + S - 1; q_pos and
+    key_lens (int32 CUDA [B]) are global: query row i of sequence b sits at
+    q_pos[b] + i, keys below key_lens[b] are valid.  Returns (o, lse) of this
+    shard alone, to be combined with attn_lse_merge."""
+    lib = load()
+    B, Hq, T, D = q.shape
+    Bk, Hkv, S, Dk = k.shape
+    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q/k/v shape mismatch")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    dt = _dtype_code(q)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, T), device=q.device, dtype=torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if tuple(o.shape) != tuple(q.shape) or lse.numel() != B * Hq * T:
+        raise ValueError("o must have q's shape and lse B*Hq*T floats")
+    if q_pos.numel() != B or key_lens.numel() != B:
+        raise ValueError("q_pos and key_lens must have B entries")
+    rc = lib.attn_fwd_kv_shard(_dev(q, "q", ndim=4), _dev(k, "k", ndim=4), _dev(v, "v", ndim=4),
+                               _dev(o, "o", dtype=q.dtype, ndim=4),
+                               _dev(lse, "lse", dtype=torch.float32),
+                               _dev(q_pos, "q_pos", dtype=torch.int32, ndim=1),
+                               _dev(key_lens, "key_lens", dtype=torch.int32, ndim=1),
+                               int(k_off), B, Hq, Hkv, T, S, D, dt, int(bool(causal)),
+                               float(scale), _stream(stream))
+    _check(rc, "attn_fwd_kv_shard")
+    return o, lse
+
+
+def attn_lse_merge(o_parts, lse_parts, o=None, lse=None, stream=None):
+    """Merge partials over disjoint key sets: o_parts [N,B,Hq,T,D] (bf16, fp16
+    or fp32), lse_parts float32 [N,B,Hq,T] -> (o [B,Hq,T,D], lse [B,Hq,T])."""
+    lib = load()
+    N, B, Hq, T, D = o_parts.shape
+    if tuple(lse_parts.shape) != (N, B, Hq, T):
+        raise ValueError("lse_parts must be [N,B,Hq,T]")
+    if o is None:
+        o = torch.empty(o_parts.shape[1:], device=o_parts.device, dtype=o_parts.dtype)
+    if lse is None:
+        lse = torch.empty((B, Hq, T), device=o_parts.device, dtype=torch.float32)
+    if tuple(o.shape) != tuple(o_parts.shape[1:]) or lse.numel() != B * Hq * T:
+        raise ValueError("o must be [B,Hq,T,D] and lse B*Hq*T floats")
+    rc = lib.attn_lse_merge(_dev(o_parts, "o_parts", ndim=5),
+                            _dev(lse_parts, "lse_parts", dtype=torch.float32, ndim=4), N,
+                            _dev(o, "o", dtype=o_parts.dtype, ndim=4),
+                            _dev(lse, "lse", dtype=torch.float32), B, Hq, T, D,
+                            _dtype_code(o_parts), _stream(stream))
+    _check(rc, "attn_lse_merge")
     return o, lse
 
 

@@ -22,6 +22,7 @@
 #include "decode.cuh"
 #include "fwd_bf16_tc.cuh"
 #include "fwd_f32.cuh"
+#include "merge.cuh"
 
 namespace {
 
@@ -166,7 +167,7 @@ template <int D, bool kF16, bool kF8 = false>
 int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                   int Hq, int Hkv, int T, int S, int causal, const int32_t* key_lens,
                   const int32_t* q_pos, float scale, cudaStream_t st,
-                  const float* qkv_descale = nullptr) {
+                  const float* qkv_descale = nullptr, int k_off = 0, bool shard = false) {
   using namespace attn::tcfwd;
   using C = Cfg<D, kF8 ? 1 : 2>;
   static std::atomic<uint64_t> smem_done{0};
@@ -195,6 +196,8 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* l
   p.T = T;
   p.S = S;
   p.causal = causal ? 1 : 0;
+  p.k_off = k_off;
+  p.shard = shard ? 1 : 0;
   // Pair slots per (batch, head): a sequence whose count of query tiles
   // with a non-padded row is odd has its pairs shifted 128 rows down, so it
   // needs room for T + 128 rows.  Without key_lens and q_pos every sequence
@@ -224,7 +227,7 @@ int launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* l
 template <int NC>
 int launch_fwd_f32(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                    int Hq, int Hkv, int T, int S, int D, int causal, const int32_t* key_lens,
-                   const int32_t* q_pos, float scale, cudaStream_t st) {
+                   const int32_t* q_pos, float scale, cudaStream_t st, int k_off, bool shard) {
   using namespace attn::f32fwd;
   static std::atomic<uint64_t> smem_done{0};
   auto kernel = fwd_f32_kernel<NC>;
@@ -245,6 +248,8 @@ int launch_fwd_f32(const void* q, const void* k, const void* v, void* o, float* 
   p.S = S;
   p.D = D;
   p.causal = causal ? 1 : 0;
+  p.k_off = k_off;
+  p.shard = shard ? 1 : 0;
   p.scale = scale;
   dim3 grid((T + kBM - 1) / kBM, Hq, B);
   kernel<<<grid, kWarps * 32, smem, st>>>(p);
@@ -298,15 +303,22 @@ int launch_decode_g(const attn::decode::Params& p, cudaStream_t st) {
     auto kernel = decode_split_mma_kernel<D, G, kF16>;
     if (!ensure_smem(kernel, C::kSmemBytes, smem_done)) return ATTN_ERR_CUDA;
     const long long rows = (long long)p.B * p.Hkv * p.S_max;
-    if (rows >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+    if (rows + kSubKeys >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
     CUtensorMap tk, tv;
     if (!make_tmap_bf16_2d(&tk, p.kc, D, rows, C::kSub, kF16) ||
         !make_tmap_bf16_2d(&tv, p.vc, D, rows, C::kSub, kF16))
       return ATTN_ERR_CUDA;
-    const long long items = (long long)p.splits * p.B * p.Hkv;
-    long long ctas = std::min<long long>(num_sms(), (items + C::kWarps - 1) / C::kWarps);
-    if (ctas < 1) ctas = 1;
+    // Persistent: one CTA per SM at most, enough warps that every warp's
+    // span can hold >= kMinSpan sub-tiles when the cache is full.
+    const long long subtiles = (long long)p.B * p.Hkv * ((p.S_max + kSubKeys - 1) / kSubKeys);
+    const long long want = (subtiles / kMinSpan + C::kWarps - 1) / C::kWarps;
+    const long long ctas = std::max<long long>(1, std::min<long long>(num_sms(), want));
     launch_pdl(kernel, dim3((unsigned)ctas), dim3(32 * C::kWarps), C::kSmemBytes, st, tk, tv, p);
+    if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
+    const long long heads = (long long)p.B * p.Hq;  // one warp each
+    launch_pdl(decode_combine_spans_kernel<T, D>, dim3((unsigned)((heads + 7) / 8)), dim3(256), 0,
+               st, p);
+    return launch_status();
   } else {
     // fp32: one block per (chunk, kv head, sequence) on the CUDA cores
     static std::atomic<uint64_t> smem_done{0};
@@ -335,11 +347,13 @@ int launch_decode_d(const attn::decode::Params& p, int G, cudaStream_t st) {
 
 bool finite_positive(float x) { return std::isfinite(x) && x > 0.f; }
 
-// Shared by attn_fwd and attn_fwd_chunked: validation and kernel choice.
+// Shared by attn_fwd, attn_fwd_chunked and attn_fwd_kv_shard: validation and
+// kernel choice.  `shard`: key_lens and q_pos are global positions and the
+// keys start at global position k_off (common.cuh, seq_geom).
 int fwd_dispatch(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                  int Hq, int Hkv, int T, int S, int D, int dtype, int causal,
                  const int32_t* key_lens, const int32_t* q_pos, float scale,
-                 attn_stream_t stream) {
+                 attn_stream_t stream, int k_off = 0, bool shard = false) {
   if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || S <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0 || !finite_positive(scale)) return ATTN_ERR_INVALID_ARG;
@@ -355,7 +369,7 @@ int fwd_dispatch(const void* q, const void* k, const void* v, void* o, float* ls
     const bool f16 = dtype == ATTN_F16;
 #define ATTN_TC_CASE(DD, F)                                                                  \
   return launch_fwd_tc<DD, F>(q, k, v, o, lse, B, Hq, Hkv, T, S, causal, key_lens, q_pos, \
-                              scale, st);
+                              scale, st, nullptr, k_off, shard);
     if (D == 64) {
       if (f16) ATTN_TC_CASE(64, true) else ATTN_TC_CASE(64, false)
     }
@@ -369,7 +383,7 @@ int fwd_dispatch(const void* q, const void* k, const void* v, void* o, float* ls
 #define ATTN_F32_CASE(N)                                                                    \
   case N:                                                                                   \
     return launch_fwd_f32<N>(q, k, v, o, lse, B, Hq, Hkv, T, S, D, causal, key_lens, q_pos, \
-                             scale, st);
+                             scale, st, k_off, shard);
     switch (nc) {
       ATTN_F32_CASE(1) ATTN_F32_CASE(2) ATTN_F32_CASE(3) ATTN_F32_CASE(4)
       ATTN_F32_CASE(5) ATTN_F32_CASE(6) ATTN_F32_CASE(7) ATTN_F32_CASE(8)
@@ -435,6 +449,49 @@ int attn_fwd_chunked(const void* q, const void* kcache, const void* vcache, void
                       q_pos, scale, stream);
 }
 
+int attn_fwd_kv_shard(const void* q, const void* k, const void* v, void* o, float* lse,
+                      const int32_t* q_pos, const int32_t* key_lens, int k_off, int B, int Hq,
+                      int Hkv, int T, int S, int D, int dtype, int causal, float scale,
+                      attn_stream_t stream) {
+  if (!q_pos || !key_lens || k_off < 0) return ATTN_ERR_INVALID_ARG;
+  if (k_off >= (1 << 30) || T >= (1 << 30) || S >= (1 << 30)) return ATTN_ERR_UNSUPPORTED;
+  return fwd_dispatch(q, k, v, o, lse, B, Hq, Hkv, T, S, D, dtype, causal, key_lens, q_pos,
+                      scale, stream, k_off, true);
+}
+
+int attn_lse_merge(const void* o_parts, const float* lse_parts, int n_parts, void* o, float* lse,
+                   int B, int Hq, int T, int D, int dtype, attn_stream_t stream) {
+  if (!o_parts || !lse_parts || !o) return ATTN_ERR_INVALID_ARG;
+  if (n_parts <= 0 || B <= 0 || Hq <= 0 || T <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  size_t esz;
+  if (dtype == ATTN_BF16 || dtype == ATTN_F16) esz = 2;
+  else if (dtype == ATTN_F32) esz = 4;
+  else return ATTN_ERR_INVALID_ARG;
+  if ((size_t)D * esz % 16 != 0 || D > 1024) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned16(o_parts) || !aligned16(o) || !aligned4(lse_parts) ||
+      (lse != nullptr && !aligned4(lse)))
+    return ATTN_ERR_INVALID_ARG;
+  attn::merge::Params p;
+  p.o_parts = o_parts;
+  p.lse_parts = lse_parts;
+  p.o = o;
+  p.lse = lse;
+  p.rows = (long long)B * Hq * T;
+  p.n_parts = n_parts;
+  p.D = D;
+  const long long threads = p.rows * (long long)((size_t)D * esz / 16);
+  const long long blocks = std::max<long long>(
+      1, std::min<long long>((threads + 255) / 256, (long long)num_sms() * 16));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (dtype == ATTN_BF16)
+    attn::merge::lse_merge_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(p);
+  else if (dtype == ATTN_F16)
+    attn::merge::lse_merge_kernel<__half><<<(unsigned)blocks, 256, 0, st>>>(p);
+  else
+    attn::merge::lse_merge_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(p);
+  return launch_status();
+}
+
 size_t attn_bwd_workspace_size(int B, int Hq, int T) {
   if (B <= 0 || Hq <= 0 || T <= 0) return 0;
   return ((size_t)B * Hq * T * sizeof(float) + 15) / 16 * 16;
@@ -489,7 +546,10 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
 
 size_t attn_decode_workspace_size(int B, int Hq, int S_max, int D) {
   if (B <= 0 || Hq <= 0 || S_max <= 0 || D <= 0) return 0;
-  return (size_t)B * Hq * attn::decode::max_splits(S_max) * ((size_t)D + 2) * sizeof(float);
+  // per (b, h): partial_slots partials of D + 2 floats (O, maximum,
+  // denominator); then the split plan: B + 2 int64 (prefix sums, warp count)
+  return (size_t)B * Hq * attn::decode::partial_slots(S_max) * ((size_t)D + 2) * sizeof(float) +
+         ((size_t)B + 2) * sizeof(long long);
 }
 
 }  // extern "C"
@@ -541,11 +601,12 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, const int
   p.Hq = Hq;
   p.Hkv = Hkv;
   p.S_max = S_max;
-  p.splits = attn::decode::max_splits(S_max);
+  p.splits = attn::decode::partial_slots(S_max);
   const size_t slots = (size_t)B * Hq * p.splits;
   p.ws_o = static_cast<float*>(workspace);
   p.ws_m = p.ws_o + slots * D;
   p.ws_l = p.ws_m + slots;
+  p.plan = reinterpret_cast<long long*>(p.ws_l + slots);  // 8-byte aligned: D + 2 is even
   p.scale_log2 = scale * kLog2e;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (dtype == ATTN_BF16) {

@@ -389,6 +389,42 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ---------------------------------------------------- prefill geometry
+
+// Per-sequence geometry of a prefill over the keys [k_off, k_off + S) of a
+// sequence (k_off = 0 and the whole sequence unless the keys are sharded).
+// In the sequence's own (global) key positions: query row i sits at
+// position offg + i, where offg = q_pos[b] (chunked prefill, sharded keys)
+// or S - T (bottom-right alignment); key position x is visible to it iff
+// x < Lg and (!causal or x <= offg + i), with Lg = key_lens[b] (S when
+// there are none; clamped to [0, S] unless the keys are sharded, where it is
+// the global length); row i is a padded row iff offg + i >= Lg.  In the
+// shard's local key index j = x - k_off this becomes:
+//   L    visible local keys are j < L             (L = clamp(Lg - k_off, 0, S))
+//   off  row i sits at local position i + off     (off = offg - k_off, clamped
+//        to [-(T + 256), S], which changes no visibility: below, the row sees
+//        nothing; above, every key of the shard below L)
+//   R    rows i < R are not padded                (R = clamp(Lg - offg, 0, T))
+// Global positions are taken clamped to [-2^30, 2^30] (sizes and k_off are
+// below 2^30), so every difference above fits in 32 bits; no sequence comes
+// near those bounds.
+struct SeqGeom {
+  int L, off, R;
+};
+constexpr int kPosLimit = 1 << 30;
+__device__ __forceinline__ SeqGeom seq_geom(const int32_t* key_lens, const int32_t* q_pos,
+                                            int k_off, bool shard, int b, int T, int S) {
+  int Lg = S;
+  if (key_lens != nullptr)
+    Lg = shard ? min(max(key_lens[b], -kPosLimit), kPosLimit) : min(max(key_lens[b], 0), S);
+  const int offg = q_pos != nullptr ? min(max(q_pos[b], -kPosLimit), kPosLimit) : S - T;
+  SeqGeom g;
+  g.L = min(max(Lg - k_off, 0), S);
+  g.off = min(max(offg - k_off, -(T + 256)), S);
+  g.R = min(max(Lg - offg, 0), T);
+  return g;
+}
+
 // ------------------------------------------------------------- numerics
 
 __device__ __forceinline__ float ex2_approx(float x) {

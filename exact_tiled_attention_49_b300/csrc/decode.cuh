@@ -7,15 +7,21 @@
 // (Cost model).  Grouped-query attention lets the G = Hq / Hkv query heads of
 // one KV head share a single read of its K and V rows.
 //
-// Work is cut into items (chunk of kChunk keys, kv head, sequence); each item
-// is reduced to one partial result per query head: the chunk maximum m (log2
-// units), the denominator l and the unnormalised output O.
+// Each (sequence, KV head) is a stream of cached keys.  Pieces of the streams
+// are reduced independently to one partial result per query head: the
+// piece's maximum m (log2 units), the denominator l and the unnormalised
+// output O.
 //   bf16: decode_split_mma_kernel -- persistent streaming warps on the tensor
-//         cores (mma.sync m16n8k16), K/V streamed by TMA.
-//   fp32: decode_split_kernel -- one block per item on the CUDA cores, exact
-//         float32 arithmetic.
-// Pass 2 (decode_combine_kernel) merges the partials of every chunk with the
-// online-softmax rescaling exp2(m_chunk - m_max) ("Implementing attention
+//         cores (mma.sync m16n8k16), K/V streamed by TMA.  All streams, laid
+//         end to end in 32-key sub-tiles, are cut into one contiguous,
+//         equal span per warp, so every warp reads the same number of bytes
+//         whatever the lengths; a warp carries its running softmax across
+//         chunks and writes one partial per stream it touches.
+//   fp32: decode_split_kernel -- one block per 256-key chunk on the CUDA
+//         cores, exact float32 arithmetic.
+// Pass 2 (decode_combine_spans_kernel, or decode_combine_kernel after the
+// fp32 split) merges the partials of every piece with the
+// online-softmax rescaling exp2(m_piece - m_max) ("Implementing attention
 // from scratch", Stable softmax), normalises, and writes O and LSE.
 #pragma once
 
@@ -26,11 +32,18 @@
 namespace attn {
 namespace decode {
 
-constexpr int kChunk = 256;  // keys per work item (one partial per item)
+constexpr int kChunk = 256;  // fp32 kernel: keys per block (one partial per chunk)
 constexpr int kWarps = 8;    // fp32 kernel: 32 keys per warp
 constexpr int kThreads = kWarps * 32;
+constexpr int kSubKeys = 32;  // bf16 kernel: keys per sub-tile (the unit of the split)
+constexpr int kMinSpan = 8;   // bf16 kernel: sub-tiles per warp at least (256 keys)
 
 __host__ __device__ constexpr int max_splits(int S_max) { return (S_max + kChunk - 1) / kChunk; }
+
+// Partial slots per (sequence, query head).  fp32: one per 256-key chunk.
+// bf16: a stream of n <= ceil(S_max / 32) sub-tiles meets at most
+// floor((n - 2) / 8) + 2 <= ceil(S_max / 256) + 1 spans of >= 8 sub-tiles.
+__host__ __device__ constexpr int partial_slots(int S_max) { return max_splits(S_max) + 1; }
 
 struct Params {
   const void* q;        // [B,Hq,D]
@@ -42,9 +55,23 @@ struct Params {
   float* ws_o;          // [B,Hq,splits,D]
   float* ws_m;          // [B,Hq,splits]
   float* ws_l;          // [B,Hq,splits]
-  int B, Hq, Hkv, S_max, splits;
+  long long* plan;      // bf16 split: [B + 2] prefix sums of sub-tiles per KV head,
+                        // then the number of warps that took a span
+  int B, Hq, Hkv, S_max, splits;  // splits = partial slots per (b, h)
   float scale_log2;     // scale * log2(e)
 };
+
+// 32-key sub-tiles of a stream of L keys.
+__device__ __forceinline__ int n_sub(int L) { return (L + kSubKeys - 1) / kSubKeys; }
+
+// The span of stream keys (in sub-tiles) warp w of W takes: [w N / W, (w+1) N / W).
+// The warp whose span holds sub-tile f is the largest w with w N / W <= f.
+__device__ __forceinline__ long long span_begin(long long w, long long N, long long W) {
+  return w * N / W;
+}
+__device__ __forceinline__ long long span_owner(long long f, long long N, long long W) {
+  return ((f + 1) * W - 1) / N;
+}
 
 template <typename T> struct Vec;
 template <> struct Vec<__nv_bfloat16> { static constexpr int kPer16B = 8; };
@@ -217,13 +244,24 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Params p) {
 // ---------------------------------------------------------------------------
 // bf16 / fp16 pass 1: persistent streaming workers on the tensor cores.
 //
-// Item virtual index is chunk-major, i = chunk * (B * Hkv) + b * Hkv + g;
-// items whose chunk starts at or past kv_lens[b] are skipped.  Every warp of
-// the grid is an independent worker taking items w, w + W, w + 2W, ... (W
-// workers).  A worker streams its items' keys as 32-key sub-tiles through a
-// private 3-stage ring: K and V arrive as 128B-swizzled TMA tiles (32 rows x
-// 64 columns), the item's q rows by a bulk copy when a new item starts, and
-// two sub-tiles are in flight while the third is computed.
+// The streams of (sequence b, KV head g), in that order, are laid end to end
+// as 32-key sub-tiles: stream (b, g) holds n_b = ceil(L_b / 32) of them and
+// starts at sub-tile Hkv * P_b + g * n_b, P_b = n_0 + ... + n_{b-1}.  With N
+// sub-tiles in all and W workers (warps), worker w takes the contiguous span
+// [w N / W, (w + 1) N / W): every worker reads the same number of K/V bytes,
+// give or take one sub-tile, whatever the lengths.  W is cut down to N / 8
+// when the cache is small, so that every span holds >= 8 sub-tiles; a
+// stream then meets at most ceil(S_max / 256) + 1 spans, which bounds the
+// partial slots.  A worker carries its online softmax across the sub-tiles
+// of one stream and writes one partial per stream it touches, into the slot
+// numbered by its place among the workers that share that stream.  Every
+// worker computes the prefix sums itself (one pass over the lengths); worker
+// 0 also stores them, and the worker count, for the combine.
+//
+// A worker streams its span as 32-key sub-tiles through a private 3-stage
+// ring: K and V arrive as 128B-swizzled TMA tiles (32 rows x 64 columns),
+// the stream's q rows by a bulk copy when a stream starts, and two
+// sub-tiles are in flight while the third is computed.
 //
 // Per sub-tile: S = Q K^T with the G query heads as the M = 16 rows of
 // mma.m16n8k16 (rows past G are zero) and K fragments from ldmatrix; the
@@ -234,38 +272,32 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Params p) {
 // ldmatrix.trans.  Scores are scaled in fp32 (scale * log2 e) so that q keeps
 // its exact input values.
 struct Cursor {
-  int item;  // virtual item index, or -1 when the worker's stream is exhausted
-  int j;     // 32-key sub-tile within the item
-  int b, g, chunk, k_begin, k_end, nsub;
+  long long f;    // sub-tile index over all streams
+  long long pb;   // P_b: sub-tiles per KV head of the sequences before b
+  int b, g, j;    // sequence, KV head, sub-tile within the stream
+  int n, L;       // sub-tiles and keys of sequence b's streams
+  bool start;     // first sub-tile of a piece (stream start or span start)
 };
 
-__device__ __forceinline__ void cursor_seek(const Params& p, int n_virtual, int stride, int i,
-                                            Cursor& c) {
-  const int bh = p.B * p.Hkv;
-  for (; i < n_virtual; i += stride) {
-    const int chunk = i / bh, bg = i - chunk * bh;
-    const int b = bg / p.Hkv;
-    const int L = min(max(__ldg(p.kv_lens + b), 0), p.S_max);
-    const int k0 = chunk * kChunk;
-    if (k0 < L) {
-      c.item = i;
-      c.j = 0;
-      c.b = b;
-      c.g = bg - b * p.Hkv;
-      c.chunk = chunk;
-      c.k_begin = k0;
-      c.k_end = min(L, k0 + kChunk);
-      c.nsub = (c.k_end - k0 + 31) / 32;
-      return;
-    }
-  }
-  c.item = -1;
+__device__ __forceinline__ int seq_len(const Params& p, int b) {
+  return min(max(__ldg(p.kv_lens + b), 0), p.S_max);
 }
 
-__device__ __forceinline__ void cursor_next(const Params& p, int n_virtual, int stride,
-                                            Cursor& c) {
-  if (++c.j < c.nsub) return;
-  cursor_seek(p, n_virtual, stride, c.item + stride, c);
+// Next sub-tile of the stream order (streams with no key are skipped).
+__device__ __forceinline__ void cursor_next(const Params& p, Cursor& c) {
+  ++c.f;
+  c.start = false;
+  if (++c.j < c.n) return;
+  c.j = 0;
+  c.start = true;
+  if (++c.g < p.Hkv) return;
+  c.g = 0;
+  c.pb += c.n;
+  for (++c.b; c.b < p.B; ++c.b) {
+    c.L = seq_len(p, c.b);
+    c.n = n_sub(c.L);
+    if (c.n > 0) return;
+  }
 }
 
 template <int D, int G>
@@ -323,6 +355,16 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) {
   return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// Inclusive prefix sum over the warp's lanes.
+__device__ __forceinline__ long long warp_incl_scan(long long v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long u = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += u;
+  }
+  return v;
+}
+
 // kF16: fp16 cache and query (else bf16).
 template <int D, int G, bool kF16>
 __global__ void __launch_bounds__(32 * MmaCfg<D, G>::kWarps)
@@ -353,15 +395,62 @@ __global__ void __launch_bounds__(32 * MmaCfg<D, G>::kWarps)
 
   const int workers = gridDim.x * C::kWarps;
   const int worker = blockIdx.x * C::kWarps + warp;
-  const int n_virtual = max_splits(p.S_max) * p.B * p.Hkv;
-  Cursor pf, cc;  // prefetch cursor (two sub-tiles ahead) and compute cursor
-  cursor_seek(p, n_virtual, workers, worker, pf);
-  cc = pf;
-  int t_issue = 0, items_issued = 0;
+
+  // Sub-tiles per KV head over all sequences (worker 0 stores the prefix
+  // sums for the combine), then this worker's span.
+  long long total = 0;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    const int b = b0 + lane;
+    const long long n = b < p.B ? n_sub(seq_len(p, b)) : 0;
+    const long long incl = warp_incl_scan(n, lane);
+    if (worker == 0 && b < p.B) p.plan[b] = total + incl - n;
+    total += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  const long long N = total * p.Hkv;
+  const long long W = min((long long)workers, max(1ll, N / kMinSpan));
+  if (worker == 0 && lane == 0) {
+    p.plan[p.B] = total;
+    p.plan[p.B + 1] = W;
+  }
+  if (worker >= W || N == 0) return;
+  const long long f_begin = span_begin(worker, N, W), f_end = span_begin(worker + 1, N, W);
+
+  // Locate the first sub-tile: the sequence b whose streams hold f_begin.
+  Cursor cc;
+  {
+    long long pre = 0;
+    int found = -1;
+    long long pb = 0;
+    for (int b0 = 0; b0 < p.B && found < 0; b0 += 32) {
+      const int b = b0 + lane;
+      const long long n = b < p.B ? n_sub(seq_len(p, b)) : 0;
+      const long long incl = warp_incl_scan(n, lane);
+      const long long lo = (pre + incl - n) * p.Hkv, hi = (pre + incl) * p.Hkv;
+      const uint32_t hit = __ballot_sync(0xffffffffu, n > 0 && lo <= f_begin && f_begin < hi);
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        found = b0 + l;
+        pb = __shfl_sync(0xffffffffu, pre + incl - n, l);
+      }
+      pre += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (found < 0) return;  // cannot happen for f_begin < N; keeps every read in range
+    cc.b = found;
+    cc.pb = pb;
+    cc.L = seq_len(p, found);
+    cc.n = n_sub(cc.L);
+    const long long r = f_begin - pb * p.Hkv;
+    cc.g = (int)(r / cc.n);
+    cc.j = (int)(r - (long long)cc.g * cc.n);
+    cc.f = f_begin;
+    cc.start = true;
+  }
+  Cursor pf = cc;  // prefetch cursor, two sub-tiles ahead of the compute cursor
+  int t_issue = 0, runs_issued = 0;
 
   auto issue = [&](const Cursor& c) {
     if (lane == 0) {
-      const int row = (c.b * p.Hkv + c.g) * p.S_max + c.k_begin + 32 * c.j;
+      const int row = (c.b * p.Hkv + c.g) * p.S_max + kSubKeys * c.j;
       const int st = t_issue % C::kStages;
       const uint32_t bar = bar_full + 8 * st;
       const uint32_t dst = ring + st * C::kStageBytes;
@@ -371,8 +460,8 @@ __global__ void __launch_bounds__(32 * MmaCfg<D, G>::kWarps)
         tma_load_2d(dst + ch * C::kTileBytes, &tm_k, bar, ch * 64, row);
         tma_load_2d(dst + C::kKBytes + ch * C::kTileBytes, &tm_v, bar, ch * 64, row);
       }
-      if (c.j == 0) {  // a new item: its q rows too
-        const int qb = items_issued & 1;
+      if (c.start) {  // a new piece: its q rows too
+        const int qb = runs_issued & 1;
         mbar_arrive_expect_tx(bar_q + 8 * qb, C::kQRawBytes);
         bulk_load(qraw + qb * C::kQRawStride,
                   reinterpret_cast<const uint16_t*>(p.q) +
@@ -380,25 +469,25 @@ __global__ void __launch_bounds__(32 * MmaCfg<D, G>::kWarps)
                   C::kQRawBytes, bar_q + 8 * qb);
       }
     }
-    if (c.j == 0) ++items_issued;
+    if (c.start) ++runs_issued;
     ++t_issue;
   };
-  for (int k = 0; k < C::kStages - 1 && pf.item >= 0; ++k) {
+  for (int k = 0; k < C::kStages - 1 && pf.f < f_end; ++k) {
     issue(pf);
-    cursor_next(p, n_virtual, workers, pf);
+    cursor_next(p, pf);
   }
 
-  uint32_t qa[KS][4];        // Q fragments (rows = heads), fixed per item
+  uint32_t qa[KS][4];        // Q fragments (rows = heads), fixed per piece
   float o[NT][4];            // O accumulator fragments
   float m_run[2], l_run[2];  // rows gr and gr + 8 (log2 units)
-  int t = 0, item_seq = 0;
+  int t = 0, run_seq = 0;
   bool ok = true;
   const float sl2 = p.scale_log2;
-  while (cc.item >= 0 && ok) {
-    if (cc.j == 0) {
-      // new item: Q fragments from its q rows; reset the running state
-      const int qb = item_seq & 1;
-      ok = mbar_wait(bar_q + 8 * qb, (item_seq >> 1) & 1, 0x29);
+  while (cc.f < f_end && ok) {
+    if (cc.start) {
+      // new piece: Q fragments from its q rows; reset the running state
+      const int qb = run_seq & 1;
+      ok = mbar_wait(bar_q + 8 * qb, (run_seq >> 1) & 1, 0x29);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       const uint8_t* qs = smem + C::kOffQRaw + qb * C::kQRawStride;
@@ -418,25 +507,25 @@ __global__ void __launch_bounds__(32 * MmaCfg<D, G>::kWarps)
       for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
       m_run[0] = m_run[1] = -INFINITY;
       l_run[0] = l_run[1] = 0.f;
-      ++item_seq;
+      ++run_seq;
       __syncwarp();
     }
-    if (pf.item >= 0) {  // keep two sub-tiles in flight
+    if (pf.f < f_end) {  // keep two sub-tiles in flight
       issue(pf);
-      cursor_next(p, n_virtual, workers, pf);
+      cursor_next(p, pf);
     }
     const int st = t % C::kStages;
     ok = mbar_wait(bar_full + 8 * st, (t / C::kStages) & 1, 0x2a);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
-    const int nkeys = min(32, cc.k_end - (cc.k_begin + 32 * cc.j));
+    const int nkeys = min(kSubKeys, cc.L - kSubKeys * cc.j);
     const uint32_t kst = ring + st * C::kStageBytes;
     const uint32_t vst = kst + C::kKBytes;
-    if (nkeys < 32) {
+    if (nkeys < kSubKeys) {
       // V rows past the sequence end may hold anything (NaN included): clear
       // them so that 0 * garbage cannot reach O
       uint8_t* vt = smem + C::kOffRing + st * C::kStageBytes + C::kKBytes;
-      const int per_chunk = (32 - nkeys) * 8;
+      const int per_chunk = (kSubKeys - nkeys) * 8;
       for (int idx = lane; idx < per_chunk * C::kChunks; idx += 32) {
         const int ch = idx / per_chunk, rem = idx - ch * per_chunk;
         *reinterpret_cast<uint4*>(vt + ch * C::kTileBytes + (nkeys + rem / 8) * 128 +
@@ -519,8 +608,11 @@ __global__ void __launch_bounds__(32 * MmaCfg<D, G>::kWarps)
     }
     __syncwarp();  // the stage may be refilled from here on
 
-    if (cc.j + 1 == cc.nsub) {
-      // end of the item: one partial per query head of the group
+    if (cc.j + 1 == cc.n || cc.f + 1 == f_end) {
+      // end of a piece: one partial per query head of the group, in the slot
+      // numbered by this worker's place among the workers of the stream
+      const long long s0 = cc.pb * p.Hkv + (long long)cc.g * cc.n;  // stream start
+      const int slot = worker - (int)span_owner(s0, N, W);
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         float l = l_run[r];
@@ -528,20 +620,19 @@ __global__ void __launch_bounds__(32 * MmaCfg<D, G>::kWarps)
         l += __shfl_xor_sync(0xffffffffu, l, 2);
         const int h = gr + 8 * r;
         if (h < G) {
-          const size_t slot =
-              ((size_t)cc.b * p.Hq + (size_t)cc.g * G + h) * p.splits + cc.chunk;
+          const size_t idx = ((size_t)cc.b * p.Hq + (size_t)cc.g * G + h) * p.splits + slot;
 #pragma unroll
           for (int n = 0; n < NT; ++n)
-            *reinterpret_cast<float2*>(p.ws_o + slot * D + n * 8 + 2 * tq) =
+            *reinterpret_cast<float2*>(p.ws_o + idx * D + n * 8 + 2 * tq) =
                 make_float2(o[n][2 * r], o[n][2 * r + 1]);
           if (tq == 0) {
-            p.ws_m[slot] = m_run[r];
-            p.ws_l[slot] = l;
+            p.ws_m[idx] = m_run[r];
+            p.ws_l[idx] = l;
           }
         }
       }
     }
-    cursor_next(p, n_virtual, workers, cc);
+    cursor_next(p, cc);
     ++t;
   }
   // Drain: every issued copy has landed before the warp exits (immediate
@@ -552,13 +643,81 @@ __global__ void __launch_bounds__(32 * MmaCfg<D, G>::kWarps)
       if (tt >= 0) mbar_wait(bar_full + 8 * (tt % C::kStages), (tt / C::kStages) & 1, 0x2b);
     }
     for (int k = 0; k < 2; ++k) {
-      const int ii = items_issued - 1 - k;
+      const int ii = runs_issued - 1 - k;
       if (ii >= 0) mbar_wait(bar_q + 8 * (ii & 1), (ii >> 1) & 1, 0x2c);
     }
   }
 }
 
-// Merge the chunk partials of one (b, h): grid (Hq, B), D threads.
+// Merge the partials of the bf16 split kernel: one warp per (b, h), grid of
+// ceil(B * Hq / 8) blocks of 8 warps.  The partials of (b, h) are the pieces
+// of its stream, one per worker span that met it (found from the plan the
+// split kernel stored), usually one to three: lane i reads piece i's
+// maximum and denominator, the warp reduces them, and each lane then sums
+// its D / 32 output columns over the pieces with 16-byte (D = 128) or
+// 8-byte loads.  No block barrier and few dependent loads: the merge is
+// latency bound, not bandwidth bound.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) decode_combine_spans_kernel(Params p) {
+  constexpr int C = D / 32;  // output columns per lane
+  static_assert(C == 2 || C == 4, "D is 64 or 128");
+  const int lane = threadIdx.x & 31;
+  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);  // b * Hq + h
+  grid_dependency_wait();  // the partials and the plan come from the split kernel
+  grid_dependents_launch();
+  if (row >= (long long)p.B * p.Hq) return;
+  const int b = (int)(row / p.Hq), h = (int)(row - (long long)b * p.Hq);
+  const long long nb = p.plan[b + 1] - p.plan[b];  // sub-tiles of each stream of b
+  int n = 0;
+  if (nb > 0) {
+    const long long N = p.plan[p.B] * p.Hkv, W = p.plan[p.B + 1];
+    const long long s0 = p.plan[b] * p.Hkv + (long long)(h / (p.Hq / p.Hkv)) * nb;
+    n = (int)(span_owner(s0 + nb - 1, N, W) - span_owner(s0, N, W)) + 1;
+  }
+  T* o = reinterpret_cast<T*>(p.o) + row * D + lane * C;
+  if (n == 0) {
+#pragma unroll
+    for (int c = 0; c < C; ++c) store_out(o + c, 0.f);
+    if (p.lse != nullptr && lane == 0) p.lse[row] = -INFINITY;
+    return;
+  }
+  const float* wm = p.ws_m + row * p.splits;
+  const float* wl = p.ws_l + row * p.splits;
+  const float* wo = p.ws_o + row * p.splits * D + lane * C;
+  // maximum over the pieces (n may exceed 32 for very long caches)
+  float M = -INFINITY;
+  for (int i = lane; i < n; i += 32) M = fmaxf(M, wm[i]);
+  M = warp_max(M);
+  float acc[C], l = 0.f;
+#pragma unroll
+  for (int c = 0; c < C; ++c) acc[c] = 0.f;
+  for (int base = 0; base < n; base += 32) {
+    const int i = base + lane;
+    const float sc = i < n ? exp2f(wm[i] - M) : 0.f;
+    l += i < n ? sc * wl[i] : 0.f;
+    const int cnt = min(32, n - base);
+    for (int k = 0; k < cnt; ++k) {
+      const float w = __shfl_sync(0xffffffffu, sc, k);
+      const float* src = wo + (size_t)(base + k) * D;
+      if constexpr (C == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+        acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
+      } else {
+        const float2 v = *reinterpret_cast<const float2*>(src);
+        acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+      }
+    }
+  }
+  l = warp_sum(l);
+  const float inv = 1.f / l;
+#pragma unroll
+  for (int c = 0; c < C; ++c) store_out(o + c, acc[c] * inv);
+  if (p.lse != nullptr && lane == 0) p.lse[row] = (M + log2f(l)) * 0.69314718055994531f;
+}
+
+// Merge the chunk partials of the fp32 split kernel (one per 256-key chunk)
+// of one (b, h): grid (Hq, B), D threads.
 template <typename T, int D>
 __global__ void __launch_bounds__(D) decode_combine_kernel(Params p) {
   __shared__ float sc_s[1024];
@@ -567,7 +726,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(Params p) {
   grid_dependency_wait();  // the partials come from the split kernel
   grid_dependents_launch();
   const int Lb = min(max(p.kv_lens[b], 0), p.S_max);
-  const int n = (Lb + kChunk - 1) / kChunk;
+  const int n = (Lb + kChunk - 1) / kChunk;  // partials to merge, from slot 0
   const size_t row = (size_t)b * p.Hq + h;
   T* o = reinterpret_cast<T*>(p.o) + row * D + d;
   if (n == 0) {
@@ -581,7 +740,7 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(Params p) {
   float acc = 0.f, l = 0.f, M = -INFINITY;
   for (int base = 0; base < n; base += 1024) {
     const int cnt = min(1024, n - base);
-    // maximum of this batch of chunk maxima, block-wide
+    // maximum of this batch of partial maxima, block-wide
     float mloc = -INFINITY;
     for (int s = d; s < cnt; s += D) mloc = fmaxf(mloc, wm[base + s]);
     mloc = warp_max(mloc);

@@ -97,6 +97,8 @@ struct Params {
   const int32_t* q_pos;     // [B] key position of query row 0, or null (S - T)
   int B, Hq, Hkv, T, S;
   int causal;
+  int k_off;                // global position of key row 0 (sharded keys; else 0)
+  int shard;                // key_lens / q_pos are global positions (see seq_geom)
   int n_pairs;              // pair slots per (batch, head): enough for T + 128 rows
                             // when a sequence's pairs may be shifted
   int n_items;              // n_pairs * B * Hq
@@ -110,17 +112,10 @@ struct Item {
   int b, h, q0;             // q0 = first row of query tile 0
 };
 
-// Valid key bound L of sequence b.
-__device__ __forceinline__ int key_bound(const Params& p, int b) {
-  return p.key_lens != nullptr ? min(max(p.key_lens[b], 0), p.S) : p.S;
-}
-
-// Key position of query row 0 of sequence b: S - T (bottom-right) or, for
-// chunked prefill against a cache, q_pos[b].  Clamping to [-(T + 256), S]
-// keeps the index arithmetic in range and changes nothing: below it every
-// row's position is negative, above it every row is padded.
-__device__ __forceinline__ int q_offset(const int32_t* q_pos, int b, int T, int S) {
-  return q_pos != nullptr ? min(max(q_pos[b], -(T + 256)), S) : S - T;
+// Geometry of sequence b (common.cuh, seq_geom): valid key bound L, query
+// offset off (row i sits at key i + off) and non-padded row count R.
+__device__ __forceinline__ SeqGeom geom(const Params& p, int b) {
+  return seq_geom(p.key_lens, p.q_pos, p.k_off, p.shard != 0, b, p.T, p.S);
 }
 
 // Pairing of query tiles.  The query tiles of a sequence that hold at least
@@ -130,21 +125,21 @@ __device__ __forceinline__ int q_offset(const int32_t* q_pos, int b, int T, int 
 // causal mask, instead of the last and heaviest one.  A shifted sequence's
 // first pair then has a virtual tile at rows -128..-1, which has no rows, no
 // key tiles and no loads.
-__device__ __forceinline__ int seq_shift(int T, int L, int off) {
-  const int rows = min(T, L - off);  // rows below this are not padded
+__device__ __forceinline__ int seq_shift(int T, int R) {
+  const int rows = min(T, R);  // rows below this are not padded
   const int tiles = rows > 0 ? (rows + kBM - 1) / kBM : 0;
   return (tiles & 1) ? kBM : 0;
 }
 
 // Number of key tiles the query tile starting at row q0 must visit (0 when
-// every row of the tile is past T, padded, virtual or sees no key); `off` is
-// the sequence's q_offset.  Every role computes it the same way so they
-// agree on the trip counts.
-__device__ __forceinline__ int tile_count(const Params& p, int q0, int L, int off) {
+// every row of the tile is past T, padded, virtual or sees no key), for the
+// sequence geometry g.  Every role computes it the same way so they agree on
+// the trip counts.
+__device__ __forceinline__ int tile_count(const Params& p, int q0, const SeqGeom& g) {
   if (q0 < 0 || q0 >= p.T) return 0;
-  if (q0 + off >= L) return 0;  // every row of the tile is a padded row
-  int kv_end = L;
-  if (p.causal) kv_end = min(L, q0 + kBM + off);  // last row sees keys <= q0+BM-1+off
+  if (q0 >= g.R) return 0;  // every row of the tile is a padded row
+  int kv_end = g.L;
+  if (p.causal) kv_end = min(g.L, q0 + kBM + g.off);  // last row sees keys <= q0+BM-1+off
   if (kv_end <= 0) return 0;
   return (kv_end + kBN - 1) / kBN;
 }
@@ -157,10 +152,13 @@ __device__ __forceinline__ int tile_count(const Params& p, int q0, int L, int of
 struct SchedArgs {
   const int32_t* key_lens;
   const int32_t* q_pos;
-  int n_pairs, B, Hq, T, S, causal, all_busy;
+  int n_pairs, B, Hq, T, S;
+  int flags;      // kCausal | kAllBusy | kShard
   FastDiv div_B, div_Hq;
   int shift_all;  // the shift of every sequence (closed-form walk)
+  int k_off;
 };
+enum : int { kCausal = 1, kAllBusy = 2, kShard = 4 };
 static_assert(sizeof(SchedArgs) <= 64, "SchedArgs fits its shared-memory slot");
 struct WalkState {
   int g0;         // first group of the current 32-group window
@@ -173,9 +171,9 @@ struct WalkState {
 };
 
 // Key tiles of the query tile starting at q0 (the rule of tile_count).
-__device__ __forceinline__ int sched_tiles(const SchedArgs& a, int q0, int L, int off) {
-  if (q0 < 0 || q0 >= a.T || q0 + off >= L) return 0;
-  const int kv_end = a.causal ? min(L, q0 + kBM + off) : L;
+__device__ __forceinline__ int sched_tiles(const SchedArgs& a, int q0, const SeqGeom& g) {
+  if (q0 < 0 || q0 >= a.T || q0 >= g.R) return 0;
+  const int kv_end = (a.flags & kCausal) ? min(g.L, q0 + kBM + g.off) : g.L;
   return kv_end <= 0 ? 0 : (kv_end + kBN - 1) / kBN;
 }
 
@@ -212,7 +210,7 @@ __device__ __noinline__ uint64_t sched_next(const SchedArgs* args, WalkState* st
   const int lane = threadIdx.x & 31;
   __syncwarp();
   if (lane == 0) st->round = round + 1;
-  if (a.all_busy) {
+  if (a.flags & kAllBusy) {
     __syncwarp();
     if (kEmpty || target >= n_groups * a.Hq) return 0;
     const int g = fast_div(target, a.div_Hq);
@@ -230,11 +228,11 @@ __device__ __noinline__ uint64_t sched_next(const SchedArgs* args, WalkState* st
       bool in_list = false, shifted = false;
       if (g < n_groups) {
         const int pr = fast_div(g, a.div_B), b = g - pr * a.B;
-        const int L = a.key_lens != nullptr ? min(max(a.key_lens[b], 0), a.S) : a.S;
-        const int off = q_offset(a.q_pos, b, a.T, a.S);
-        const int sh = seq_shift(a.T, L, off);
+        const SeqGeom sg = seq_geom(a.key_lens, a.q_pos, a.k_off, (a.flags & kShard) != 0, b,
+                                    a.T, a.S);
+        const int sh = seq_shift(a.T, sg.R);
         const int q0 = (a.n_pairs - 1 - pr) * kItemRows - sh;
-        const bool busy = sched_tiles(a, q0, L, off) > 0 || sched_tiles(a, q0 + kBM, L, off) > 0;
+        const bool busy = sched_tiles(a, q0, sg) > 0 || sched_tiles(a, q0 + kBM, sg) > 0;
         in_list = busy != kEmpty;
         shifted = sh != 0;
       }
@@ -362,12 +360,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     sched->Hq = p.Hq;
     sched->T = p.T;
     sched->S = p.S;
-    sched->causal = p.causal;
     sched->div_B = p.div_B;
     sched->div_Hq = p.div_Hq;
-    sched->shift_all = seq_shift(p.T, p.S, p.S - p.T);
-    sched->all_busy =
+    sched->shift_all = seq_shift(p.T, p.T);
+    sched->k_off = p.k_off;
+    const bool all_busy =
         p.key_lens == nullptr && p.q_pos == nullptr && (!p.causal || p.T <= p.S);
+    sched->flags = (p.causal ? kCausal : 0) | (all_busy ? kAllBusy : 0) | (p.shard ? kShard : 0);
   }
   if (lane == 0) walk[0] = walk[1] = WalkState{0, 0, 0, 0, 0u, 0u, {0, 0}};
   if (warp == kMmaWarp) {
@@ -395,12 +394,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       return __all_sync(0xffffffffu, w);
     };
     // Next item with key tiles to visit (false when the walk is over).
-    auto next_item = [&](Item& x, int& L, int& off, int& n0, int& n1) {
+    auto next_item = [&](Item& x, int& L, int& n0, int& n1) {
       while (unpack_item(sched_next<false>(sched, walk), x)) {
-        L = key_bound(p, x.b);
-        off = q_offset(p.q_pos, x.b, p.T, p.S);
-        n0 = tile_count(p, x.q0, L, off);
-        n1 = tile_count(p, x.q0 + kBM, L, off);
+        const SeqGeom g = geom(p, x.b);
+        L = g.L;
+        n0 = tile_count(p, x.q0, g);
+        n1 = tile_count(p, x.q0 + kBM, g);
         if (max(n0, n1) > 0) return true;
       }
       return false;
@@ -448,8 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++ring;
     };
     Item it, nx;
-    int L = 0, off = 0, n0 = 0, n1 = 0;
-    bool have = next_item(it, L, off, n0, n1);
+    int L = 0, n0 = 0, n1 = 0;
+    bool have = next_item(it, L, n0, n1);
     bool early = false;  // Q_0 and K_0 of `it` went out with the previous item
     while (ok && have) {
       const int nm = max(n0, n1);
@@ -459,8 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) load_q(it, 1);
       if (!ok) break;
       ++qi;
-      int nL = 0, noff = 0, nn0 = 0, nn1 = 0;
-      const bool have_nx = next_item(nx, nL, noff, nn0, nn1);
+      int nL = 0, nn0 = 0, nn1 = 0;
+      const bool have_nx = next_item(nx, nL, nn0, nn1);
       // With a causal diagonal (tile 1 visits one key tile more than tile 0)
       // the MMA warp starts the next item's tile 0 while tile 1 finishes
       // alone: that item's Q_0 and K_0 go out between this item's last K and
@@ -479,7 +478,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       it = nx;
       L = nL;
-      off = noff;
       n0 = nn0;
       n1 = nn1;
       have = have_nx;
@@ -556,10 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto next_item = [&](int& n0, int& n1) {
       Item x;
       while (unpack_item(sched_next<false>(sched, walk), x)) {
-        const int L = key_bound(p, x.b);
-        const int off = q_offset(p.q_pos, x.b, p.T, p.S);
-        n0 = tile_count(p, x.q0, L, off);
-        n1 = tile_count(p, x.q0 + kBM, L, off);
+        const SeqGeom g = geom(p, x.b);
+        n0 = tile_count(p, x.q0, g);
+        n1 = tile_count(p, x.q0 + kBM, g);
         if (max(n0, n1) > 0) return true;
       }
       return false;
@@ -676,13 +673,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         Item it;
     while (ok && unpack_item(sched_next<false>(sched, walk), it)) {
-      const int L = key_bound(p, it.b);
-      const int off = q_offset(p.q_pos, it.b, p.T, p.S);
+      const SeqGeom sg = geom(p, it.b);
+      const int L = sg.L, off = sg.off;
       const int q0t = it.q0 + t * kBM;
-      const int n = tile_count(p, q0t, L, off);
+      const int n = tile_count(p, q0t, sg);
       const int i = q0t + r;
       const int pos = i + off;
-      const bool row_ok = (i >= 0) && (i < p.T) && (pos < L);
+      const bool row_ok = (i >= 0) && (i < p.T) && (i < sg.R);
       const int lim = p.causal ? min(L, pos + 1) : L;  // visible keys: [0, lim)
       float m_ref = -INFINITY;  // exponent reference (log2 units)
       float l = 0.f;

@@ -34,6 +34,8 @@ struct Params {
   const int32_t* q_pos;   // [B] key position of query row 0, or null (S - T)
   int B, Hq, Hkv, T, S, D;
   int causal;
+  int k_off;              // global position of key row 0 (sharded keys; else 0)
+  int shard;              // key_lens / q_pos are global positions (see seq_geom)
   float scale;
 };
 
@@ -55,10 +57,10 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(Params p) {
   const int g = h / (p.Hq / p.Hkv);
   const int q0 = blockIdx.x * kBM;
   // Row i sits at key position i + off: bottom-right (S - T) or, for chunked
-  // prefill against a cache, q_pos[b] (clamped: see the tcgen05 kernel).
-  const int off = p.q_pos != nullptr ? min(max(p.q_pos[b], -(p.T + 256)), p.S) : p.S - p.T;
-  int L = p.S;
-  if (p.key_lens != nullptr) L = min(max(p.key_lens[b], 0), p.S);
+  // prefill against a cache, q_pos[b]; keys below L are valid; rows below R
+  // are not padded (common.cuh, seq_geom).
+  const SeqGeom sg = seq_geom(p.key_lens, p.q_pos, p.k_off, p.shard != 0, b, p.T, p.S);
+  const int off = sg.off, L = sg.L;
 
   const size_t q_base = (((size_t)b * p.Hq + h) * p.T) * D;
   const size_t kv_base = (((size_t)b * p.Hkv + g) * p.S) * D;
@@ -99,7 +101,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_f32_kernel(Params p) {
       const int rl = warp * kRowsPerWarp + r;
       const int i = q0 + rl;
       const int pos = i + off;
-      const bool row_ok = (i < p.T) && (pos < L);
+      const bool row_ok = (i < p.T) && (i < sg.R);
       const int j = k0 + lane;
       const bool vis = row_ok && (j < L) && (!p.causal || j <= pos);
       float s = -INFINITY;

@@ -163,6 +163,71 @@ ATTN_API int attn_fwd_chunked(const void* q, const void* kcache, const void* vca
                               int causal, float scale, attn_stream_t stream);
 
 /*
+ * attn_fwd_kv_shard -- the prefill over one shard of the keys: the part of
+ * sequence parallelism that runs on one GPU ("Building a causal
+ * self-attention block from scratch in PyTorch", Extending It: distributed
+ * attention, sharding Q/K/V across devices and recombining).  The keys of
+ * each sequence are split into shards; this call computes, for the given
+ * queries, the attention over the keys of one shard only, normalised over
+ * that shard, with the shard's LSE.  attn_lse_merge then combines the
+ * partials of all shards into the attention over every key.
+ *
+ * Positions are the sequence's own (global) key positions.  The shard holds
+ * keys k_off .. k_off + S - 1; query row i of sequence b sits at position
+ * p = q_pos[b] + i; L = key_lens[b] is the sequence's valid length:
+ *     key k_off + j is visible to row i  iff  k_off + j < L and
+ *                                              (!causal or k_off + j <= p)
+ *     row i is a padded row               iff  p >= L
+ * (bottom-right alignment: q_pos[b] = L - T for a sequence whose last query
+ * is its last key).  Padded rows, and rows that see no key of this shard,
+ * are written as O = 0, LSE = -inf; attn_lse_merge gives such a partial no
+ * weight.  Shard key rows at or past L - k_off are never used.
+ *
+ *   q                 [B,Hq,T,D]   dtype          (read)
+ *   k, v              [B,Hkv,S,D]  dtype          (read: the shard's keys)
+ *   o                 [B,Hq,T,D]   dtype          (written)
+ *   lse               [B,Hq,T]     float32        (written; NULL = do not emit,
+ *                                                  but the merge needs it)
+ *   q_pos, key_lens   [B]          int32, device  (read; global positions, any
+ *                                                  value; not NULL)
+ *   k_off             >= 0: global position of the shard's key row 0
+ *
+ * Supported sizes, types and alignment as for attn_fwd.  With k_off = 0, a
+ * single shard holding every key and key_lens in [0, S], this is
+ * attn_fwd_chunked.  Returns ATTN_OK, ATTN_ERR_INVALID_ARG,
+ * ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA.
+ */
+ATTN_API int attn_fwd_kv_shard(const void* q, const void* k, const void* v, void* o, float* lse,
+                               const int32_t* q_pos, const int32_t* key_lens, int k_off, int B,
+                               int Hq, int Hkv, int T, int S, int D, int dtype, int causal,
+                               float scale, attn_stream_t stream);
+
+/*
+ * attn_lse_merge -- combines n_parts partial results of the same queries
+ * over disjoint key sets (e.g. one per key shard, from attn_fwd_kv_shard)
+ * into the attention over all those keys, by the rescaling of the online
+ * softmax ("Implementing attention from scratch", Core ideas, Stable
+ * softmax: sums kept against a running maximum are rescaled by
+ * exp(m_old - m_new)):
+ *     LSE = ln sum_n exp(LSE_n),   O = sum_n exp(LSE_n - LSE) O_n
+ * Partials with LSE_n = -inf add nothing; a row with no partial is written as
+ * O = 0, LSE = -inf.  Partials are visited in order n = 0 .. n_parts - 1
+ * with a running maximum (float32 arithmetic, output rounded once).
+ *
+ *   o_parts    [n_parts,B,Hq,T,D]  dtype    (read)
+ *   lse_parts  [n_parts,B,Hq,T]    float32  (read)
+ *   o          [B,Hq,T,D]          dtype    (written; may not alias o_parts)
+ *   lse        [B,Hq,T]            float32  (written; NULL = do not emit)
+ *
+ * Supported: dtype ATTN_BF16, ATTN_F16 or ATTN_F32 with D * element size a
+ * multiple of 16 bytes, D <= 1024; o_parts and o 16-byte aligned.  Returns
+ * ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED or ATTN_ERR_CUDA.
+ */
+ATTN_API int attn_lse_merge(const void* o_parts, const float* lse_parts, int n_parts, void* o,
+                            float* lse, int B, int Hq, int T, int D, int dtype,
+                            attn_stream_t stream);
+
+/*
  * attn_bwd_workspace_size -- bytes of device scratch attn_bwd needs: one
  * float per query row for delta = rowsum(dO * O), the row term of the
  * softmax's chain rule that the backward forms once and reads for every key

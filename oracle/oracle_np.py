@@ -275,7 +275,9 @@ def attn_bwd_magnitudes_np(q, k, v, do, causal=False, key_lens=None, scale=None,
     """Per-element magnitudes that bound the rounding error of a bf16
     evaluation of the backward (test infrastructure for tolerances).
 
-    With u = 2^-9 (one bf16 rounding), a kernel that rounds P and dS to bf16
+    With u the unit roundoff of one rounding (2^-8 for bf16: half the spacing
+    2^-7 of bf16 numbers on [1, 2); 2^-11 for fp16), a kernel that rounds P
+    and dS to bf16
     before the products, forms delta from the bf16-rounded O and rounds
     each result once has, to first order, an error of at most u times:
 

@@ -66,9 +66,10 @@ def test_status_strings(lib):
 
 
 def test_workspace_size_formula(lib):
-    # partial O (D floats) + running max + denominator per (b, h, 256-key chunk)
-    assert lib.attn_decode_workspace_size(64, 32, 8193, 128) == 64 * 32 * 33 * 130 * 4
-    assert lib.attn_decode_workspace_size(1, 1, 256, 64) == 1 * 1 * 1 * 66 * 4
+    # partial O (D floats) + running max + denominator per (b, h) and slot,
+    # ceil(S_max / 256) + 1 slots; then B + 2 int64 of the split plan
+    assert lib.attn_decode_workspace_size(64, 32, 8193, 128) == 64 * 32 * 34 * 130 * 4 + 66 * 8
+    assert lib.attn_decode_workspace_size(1, 1, 256, 64) == 1 * 1 * 2 * 66 * 4 + 3 * 8
     assert lib.attn_decode_workspace_size(0, 1, 1, 64) == 0
 
 
@@ -179,3 +180,24 @@ def test_bwd_rejects_bad_arguments(lib):
     assert bw(D=96) == 2
     assert bw(ws=None) == 3
     assert bw(ws_bytes=need - 4) == 3
+
+
+def test_kv_shard_and_merge_reject_bad_arguments(lib):
+    def sh(q_pos=FAKE, key_lens=FAKE, k_off=0, D=64, dt=1, Hq=2, Hkv=1):
+        return lib.attn_fwd_kv_shard(FAKE, FAKE, FAKE, FAKE, None, q_pos, key_lens, k_off, 1, Hq,
+                                     Hkv, 8, 16, D, dt, 1, 0.125, None)
+    assert sh(q_pos=None) == 1             # global positions are required
+    assert sh(key_lens=None) == 1
+    assert sh(k_off=-1) == 1
+    assert sh(k_off=1 << 30) == 2          # positions are limited to 2^30
+    assert sh(Hq=3, Hkv=2) == 1
+    assert sh(D=96) == 2
+    assert sh(dt=7) == 1
+
+    def mg(o_parts=FAKE, n=2, D=64, dt=1, o=FAKE):
+        return lib.attn_lse_merge(o_parts, FAKE, n, o, None, 1, 2, 8, D, dt, None)
+    assert mg(o_parts=None) == 1
+    assert mg(n=0) == 1
+    assert mg(dt=9) == 1
+    assert mg(D=4) == 2                    # 8-byte rows cannot be merged as 16-byte vectors
+    assert mg(o=MIS) == 1

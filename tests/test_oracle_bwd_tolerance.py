@@ -1,7 +1,8 @@
 """Pin of the backward's tolerance magnitudes (oracle.attn_bwd_magnitudes_np).
 
-The GPU backward's elementwise bound is u * A with u = 2^-9 (one bf16
-rounding) and A from oracle.attn_bwd_magnitudes_np.  That function claims:
+The GPU backward's elementwise bound is a small multiple of u * A, with u
+the unit roundoff of one rounding (2^-8 for bf16) and A from
+oracle.attn_bwd_magnitudes_np.  That function claims:
 a backward that rounds P (for dV = P^T dO) and dS (for dQ and dK) to bf16,
 forms delta = rowsum(dO * O) from the bf16-rounded O and rounds each result
 once has, to first order, an error of at most u * A elementwise.
@@ -34,7 +35,7 @@ import pytest
 
 import oracle
 
-U = 2.0 ** -9
+U = 2.0 ** -8   # bf16 unit roundoff
 
 CASES = [
     # (B, Hq, Hkv, T, S, D, causal, key_lens, q_pos)

@@ -62,7 +62,7 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row(E):
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(E):
-    # 64 x 32 heads x 33 chunks x (128 + 2) floats = 35 MB > 16 MiB
+    # 64 x 32 heads x 34 slots x (128 + 2) floats = 36 MB > 16 MiB
     need = E.attn_decode_workspace_size(64, 32, 8193, 128)
     assert need > E.NOALLOC_SCRATCH_BYTES
     q = torch.zeros(64, 32, 128, device="cuda", dtype=torch.bfloat16)
