@@ -77,9 +77,9 @@ PROFILED_TRAFFIC = {
     5: {"source": "exact_tiled_attention_49_b300/csrc/fwd_bf16_tc.cuh", "sha256": "103911b9e59f",
         "bytes": 1082.855168e6 + 90.0608e6, "scale": 1.0,
         "capture": "fwd_bf16_tc_kernel<128,0,0>, full workload"},
-    4: {"source": "exact_tiled_attention_49_b300/csrc/decode.cuh", "sha256": "fa78d3ab921f",
-        "bytes": 1339.557888e6 + 4.37376e6 + 2.80576e6, "scale": 1.0,
-        "capture": "decode_split_mma_kernel<128,4,0> + decode_combine_kernel, full workload"},
+    4: {"source": "exact_tiled_attention_49_b300/csrc/decode.cuh", "sha256": "517a918d784e",
+        "bytes": 1339.549184e6 + 4.434176e6 + 2.809088e6, "scale": 1.0,
+        "capture": "decode_split_mma_kernel<128,4,0> + decode_combine_spans_kernel, full workload"},
 }
 
 
@@ -521,14 +521,15 @@ def other_workloads(E, skip, device, steps, peaks):
             flush.zero_()
             run_step(E, c)
         torch.cuda.synchronize()
-        _, kern_ms, _ = time_graphs(E, c, steps, flush)
+        clk = ClockSampler(device)
+        _, kern_ms, _ = time_graphs(E, c, steps, flush, clk)
         if w.kind == "prefill":
             kl = None if c["key_lens"] is None else c["key_lens"].cpu().numpy()
             v = prefill_flops(w, kl) / (kern_ms["prefill"] * 1e-3) / 1e12
             out[str(wid)] = {"workload": w.name, "value": v, "unit": "TFLOPS",
                              "ms": kern_ms["prefill"], "kernel": "fwd_bf16_tc_kernel",
                              "frac": v / peaks["bf16_tflops"],
-                             "traffic": profiled_traffic(wid)}
+                             "traffic": profiled_traffic(wid), "clocks": clk.record()}
             if "dec" in c:
                 gbs = c["dec_bytes"] / (kern_ms["decode"] * 1e-3) / 1e9
                 out[str(wid)]["next_token_decode"] = {
@@ -540,7 +541,8 @@ def other_workloads(E, skip, device, steps, peaks):
             out[str(wid)] = {"workload": w.name, "value": v, "unit": "GB/s",
                              "ms": kern_ms["decode"], "append_ms": kern_ms["append"],
                              "kernel": "decode_split_mma_kernel+decode_combine_kernel",
-                             "frac": v / peaks["hbm_gbs"], "traffic": profiled_traffic(wid)}
+                             "frac": v / peaks["hbm_gbs"], "traffic": profiled_traffic(wid),
+                             "clocks": clk.record()}
         del c
         torch.cuda.empty_cache()
     out.update(backward_workloads(E, device, steps, peaks, flush))
@@ -927,12 +929,18 @@ def measure_block(E, args, wid, device, peaks, ws, rank, backward=False, fp8=Fal
                       / 1e9}
     del c
     torch.cuda.empty_cache()
+    return out
+
+
+def add_cpu_baseline(block, args, wid, rank, backward=False):
+    """The float64 oracle timed on the host cores for one block (rank 0).
+    Run after every GPU measurement of the line, so that no GPU timing
+    follows a long idle spell of the device."""
     if rank == 0 and not args.no_cpu_baseline:
         fn = cpu_baseline_bwd if backward else cpu_baseline
         v, unit, cores, sample = fn(wid, budget_s=args.cpu_budget)
-        out["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
-                               "sample": sample}
-    return out
+        block["cpu_baseline"] = {"value": v, "unit": unit, "cores": cores, "kind": "oracle",
+                                 "sample": sample}
 
 
 def bench_ours(args):
@@ -976,6 +984,9 @@ def bench_ours(args):
     if not args.no_other_workloads and args.batch is None:
         out["other_workloads"] = other_workloads(E, skip, device, max(3, min(args.steps, 10)),
                                                  peaks)
+    add_cpu_baseline(out, args, args.workload, rank, backward=args.backward)
+    if "decode" in out:
+        add_cpu_baseline(out["decode"], args, 4, rank)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if ws > 1:
