@@ -77,8 +77,8 @@ PROFILED_TRAFFIC = {
     5: {"source": "exact_tiled_attention_49_b300/csrc/fwd_bf16_tc.cuh", "sha256": "103911b9e59f",
         "bytes": 1082.855168e6 + 90.0608e6, "scale": 1.0,
         "capture": "fwd_bf16_tc_kernel<128,0,0>, full workload"},
-    4: {"source": "exact_tiled_attention_49_b300/csrc/decode.cuh", "sha256": "517a918d784e",
-        "bytes": 1339.549184e6 + 4.434176e6 + 2.809088e6, "scale": 1.0,
+    4: {"source": "exact_tiled_attention_49_b300/csrc/decode.cuh", "sha256": "15c773026e9f",
+        "bytes": 1339.576576e6 + 4.541696e6 + 3.42272e6, "scale": 1.0,
         "capture": "decode_split_mma_kernel<128,4,0> + decode_combine_spans_kernel, full workload"},
 }
 

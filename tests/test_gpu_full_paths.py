@@ -20,7 +20,12 @@ checks.  Each case below launches well over 2 x 148 work items:
 * bf16 D = 64 decode with 32 sequences x 8 KV heads of up to 4096 cached
   keys: every output against the oracle;
 * the backward on one sequence of the padded batch (all 16 heads, T=S=4096,
-  causal + padding), every gradient element against the float64 oracle.
+  causal + padding), every gradient element against the float64 oracle;
+* chunked prefill against ragged caches with 640 work items (sampled rows,
+  every padded row past each chunk exactly 0 / -inf);
+* decode with group sizes 16, 1 (fp16) and 8 over thousands of cached keys,
+  every output against the oracle; the exact fp32 prefill over several
+  hundred blocks.
 """
 from __future__ import annotations
 
@@ -203,3 +208,70 @@ def test_backward_padded_batch_slice(E):
     check_grad(dv, rv, av, "dv")
     assert np.all(dq.double().cpu().numpy()[~np.isfinite(rl)] == 0)
     assert torch.all(dk[:, :, L:] == 0) and torch.all(dv[:, :, L:] == 0)
+
+
+def test_chunked_prefill_many_items_sampled(E):
+    """Chunked prefill against caches (ragged cache lengths, ragged chunks)
+    with 640 work items: q_pos[b] is the cache length before the chunk,
+    kv_lens[b] = q_pos[b] + that sequence's chunk length (<= T); cache rows
+    past kv_lens hold NaN."""
+    B, Hq, Hkv, T, S_max, D = 8, 16, 4, 1024, 4096, 128
+    assert _items(B, Hq, T, True) > 2 * 148
+    g = torch.Generator(device="cuda").manual_seed(66)
+    q = torch.randn(B, Hq, T, D, generator=g, device="cuda").to(torch.bfloat16)
+    kc = torch.randn(B, Hkv, S_max, D, generator=g, device="cuda").to(torch.bfloat16)
+    vc = torch.randn(B, Hkv, S_max, D, generator=g, device="cuda").to(torch.bfloat16)
+    rng = np.random.default_rng(66)
+    qp = rng.integers(0, S_max - T + 1, size=B).astype(np.int32)
+    chunk = rng.integers(1, T + 1, size=B).astype(np.int32)
+    kl = (qp + chunk).astype(np.int32)
+    for b in range(B):
+        kc[b, :, int(kl[b]):] = float("nan")
+        vc[b, :, int(kl[b]):] = float("nan")
+    q_pos = torch.from_numpy(qp).cuda()
+    kv_lens = torch.from_numpy(kl).cuda()
+    scale = 1.0 / math.sqrt(D)
+    o, lse = E.attn_fwd_chunked(q, kc, vc, q_pos, kv_lens, scale=scale)
+    torch.cuda.synchronize()
+    assert E.attn_device_error(clear=True) == 0
+    rows = sample_rows(B, Hq, T, S_max, kl, per_head=16, seed=66, q_off=0)
+    # the rows around each sequence's chunk end too
+    extra = [(b * Hq + h) * T + i for b in range(B) for h in range(0, Hq, 5)
+             for i in (int(chunk[b]) - 1, min(int(chunk[b]), T - 1)) if 0 <= i < T]
+    rows = np.unique(np.concatenate([rows, np.array(extra, np.int64)]))
+    ro, rl = oracle_fwd(q, kc, vc, True, kv_lens, scale, rows=rows, q_pos=q_pos)
+    og, lg = gather_rows(o, lse, rows, D)
+    compare(og, lg, ro, rl, torch.bfloat16, "chunked B8 H16 T1024 S_max4096 (sampled rows)")
+    for b in range(B):   # rows past each chunk are padded rows
+        assert torch.all(o[b, :, int(chunk[b]):] == 0)
+        assert torch.all(torch.isneginf(lse[b, :, int(chunk[b]):]))
+
+
+@pytest.mark.parametrize("cfg", [(16, 32, 2, 128, "bf16"), (24, 8, 8, 64, "f16"),
+                                 (16, 64, 8, 64, "bf16")],
+                         ids=["G16-D128-bf16", "G1-D64-f16", "G8-D64-bf16"])
+def test_decode_group_sizes_at_scale(E, cfg):
+    """Decode with group sizes 16, 1 and 8 over thousands of cached keys per
+    sequence, every output against the oracle (the balanced split gives each
+    warp a span across many streams)."""
+    B, Hq, Hkv, D, dtype = cfg
+    d = workloads.decode_inputs(B, Hq, Hkv, D, 512, 6000, dtype, seed=67, device="cuda")
+    E.kv_cache_append(d["kcache"], d["vcache"], d["k_new"], d["v_new"], d["cache_len"])
+    scale = 1.0 / math.sqrt(D)
+    o, lse = E.attn_decode(d["q"], d["kcache"], d["vcache"], d["kv_len"], scale=scale)
+    torch.cuda.synchronize()
+    assert E.attn_device_error(clear=True) == 0
+    ro, rl = oracle_decode(d["q"], d["kcache"], d["vcache"], d["kv_len"], scale)
+    compare(o, lse, ro, rl, d["q"].dtype, f"decode {cfg}")
+
+
+def test_fp32_prefill_larger(E):
+    """The exact fp32 path over several hundred blocks, causal with padding."""
+    x = workloads.prefill_inputs(2, 4, 2, 700, 700, 128, "f32", seed=68, device="cuda",
+                                 lens=(300, 700))
+    scale = 1.0 / math.sqrt(128)
+    o, lse = E.attn_fwd(x["q"], x["k"], x["v"], causal=True, key_lens=x["key_lens"], scale=scale)
+    torch.cuda.synchronize()
+    assert E.attn_device_error(clear=True) == 0
+    ro, rl = oracle_fwd(x["q"], x["k"], x["v"], True, x["key_lens"], scale)
+    compare(o, lse, ro, rl, torch.float32, "fp32 B2 H4 T700 D128 causal+pad")
