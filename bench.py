@@ -613,19 +613,20 @@ def fp8_workloads(E, device, steps, peaks, flush):
 
 
 def backward_workloads(E, device, steps, peaks, flush):
-    """The backward pass (dQ, dK, dV from the saved LSE) of the long-context
-    and default prefills, one CUDA-graph replay per step with the L2
-    flushed.  Throughput counts the algorithmic 2.5x the forward's FLOPs
+    """The backward pass (dQ, dK, dV from the saved LSE) of the long-context,
+    padded-batch and short prefills, one CUDA-graph replay per step with the
+    L2 flushed.  Throughput counts the algorithmic 2.5x the forward's FLOPs
     (five products against two); the kernels compute S and dP twice, so
     they execute 3.5x."""
     import torch
     import workloads
     out = {}
-    for wid in (3, 2):
+    for wid in (3, 5, 2):
         w = workloads.WORKLOADS[wid]
         x = workloads.workload_inputs(wid, device=device)
         scale = 1.0 / math.sqrt(w.D)
-        o, lse = E.attn_fwd(x["q"], x["k"], x["v"], causal=w.causal, scale=scale)
+        kl = x["key_lens"]
+        o, lse = E.attn_fwd(x["q"], x["k"], x["v"], causal=w.causal, key_lens=kl, scale=scale)
         g = torch.Generator(device=device).manual_seed(100 + wid)
         do = torch.randn(x["q"].shape, generator=g, device=device).to(x["q"].dtype)
         ws = torch.empty(E.attn_bwd_workspace_size(w.B, w.Hq, w.T), dtype=torch.uint8,
@@ -633,8 +634,8 @@ def backward_workloads(E, device, steps, peaks, flush):
         dq, dk, dv = (torch.empty_like(x[n]) for n in ("q", "k", "v"))
 
         def step():
-            E.attn_bwd(x["q"], x["k"], x["v"], o, do, lse, causal=w.causal, scale=scale,
-                       dq=dq, dk=dk, dv=dv, workspace=ws)
+            E.attn_bwd(x["q"], x["k"], x["v"], o, do, lse, causal=w.causal, key_lens=kl,
+                       scale=scale, dq=dq, dk=dk, dv=dv, workspace=ws)
         for _ in range(3):
             step()
         graph = torch.cuda.CUDAGraph()
@@ -653,14 +654,14 @@ def backward_workloads(E, device, steps, peaks, flush):
             e1.synchronize()
             total += e0.elapsed_time(e1)
         ms = total / steps
-        flops = 2.5 * prefill_flops(w, None)
+        flops = 2.5 * prefill_flops(w, None if kl is None else kl.cpu().numpy())
         v = flops / (ms * 1e-3) / 1e12
         out[f"bwd{wid}"] = {"workload": f"backward (dQ, dK, dV) of: {w.name}", "value": v,
                             "unit": "TFLOPS", "ms": ms,
                             "kernel": "bwd_delta_kernel+bwd_dq_kernel+bwd_dkdv_kernel",
                             "frac": v / peaks["bf16_tflops"],
                             "flops": "2.5x the forward's (algorithmic)"}
-        del x, o, lse, do, ws, dq, dk, dv
+        del x, o, lse, do, ws, dq, dk, dv, kl
         torch.cuda.empty_cache()
     return out
 
