@@ -14,13 +14,14 @@ from ._lib import (ATTN_BF16, ATTN_ERR_CUDA, ATTN_F16, ATTN_ERR_INVALID_ARG,  # 
                    attn_decode_noalloc,
                    attn_bwd, attn_bwd_workspace_size,
                    attn_decode_workspace_size, attn_device_error, attn_fwd, attn_fwd_chunked,
-                   attn_fwd_fp8, attn_fwd_kv_shard, attn_lse_merge,
+                   attn_fwd_fp8, attn_fwd_host, attn_fwd_host_workspace_size,
+                   attn_fwd_kv_shard, attn_lse_merge,
                    attn_selftest_wait_timeout, ATTN_SELFTEST_ERROR,
                    attn_kernel_launches, attn_status_string, kv_cache_append, load,
                    status_string)
 
 __all__ = [
-    "attn_fwd", "attn_fwd_chunked", "attn_fwd_fp8", "attn_fwd_kv_shard", "attn_lse_merge", "attn_bwd", "attn_bwd_workspace_size", "attn_decode", "attn_decode_workspace_size", "attn_decode_noalloc",
+    "attn_fwd", "attn_fwd_host", "attn_fwd_host_workspace_size", "attn_fwd_chunked", "attn_fwd_fp8", "attn_fwd_kv_shard", "attn_lse_merge", "attn_bwd", "attn_bwd_workspace_size", "attn_decode", "attn_decode_workspace_size", "attn_decode_noalloc",
     "kv_cache_append",
     "attn_status_string", "attn_kernel_launches", "attn_device_error", "AttnError",
     "attn_selftest_wait_timeout", "ATTN_SELFTEST_ERROR",

@@ -27,6 +27,9 @@ SIGNATURES = {
                               _P]),
     "attn_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _F, _F, _F, _F,
                           _P]),
+    "attn_fwd_host_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I]),
+    "attn_fwd_host": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _P, _F, _P,
+                           ctypes.c_size_t, _P, _P, _P]),
     "attn_fwd_kv_shard": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                                _F, _P]),
     "attn_lse_merge": (_I, [_P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P]),
@@ -152,6 +155,73 @@ def attn_fwd(q, k, v, o=None, lse=None, causal=False, key_lens=None, scale=None,
     rc = lib.attn_fwd(*ptrs, lp, B, Hq, Hkv, T, S, D, dt, int(bool(causal)), kl,
                       float(scale), _stream(stream))
     _check(rc, "attn_fwd")
+    return o, lse
+
+
+def _host(t: torch.Tensor, name: str, dtype=None, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cpu":
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def attn_fwd_host_workspace_size(B, Hq, Hkv, T, S, D, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else _dtype_code(torch.empty(0, dtype=dtype))
+    return int(load().attn_fwd_host_workspace_size(B, Hq, Hkv, T, S, D, code))
+
+
+def attn_fwd_host(q, k, v, o=None, lse=None, causal=False, key_lens=None, scale=None,
+                  return_lse=True, workspace=None, stream=None, copy_in=None, copy_out=None):
+    """attn_fwd on host tensors (pinned for overlap): q [B,Hq,T,D], k/v
+    [B,Hkv,S,D] and key_lens (int32 [B] or None) on the CPU; o and lse are
+    written on the CPU (pinned ones are allocated when not given).  The
+    library copies the inputs in, computes and copies the results out in
+    pipelined stages on `stream` (compute), `copy_in` and `copy_out`
+    (torch.cuda.Stream objects; None = no overlap for that role).  Returns
+    (o, lse); they are complete once `stream` is."""
+    lib = load()
+    B, Hq, T, D = q.shape
+    Bk, Hkv, S, Dk = k.shape
+    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("q/k/v shape mismatch")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    dt = _dtype_code(q)
+    if o is None:
+        o = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, T), dtype=torch.float32, pin_memory=True)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if tuple(o.shape) != tuple(q.shape):
+        raise ValueError("o must have q's shape")
+    ptrs = [_host(q, "q", ndim=4), _host(k, "k", ndim=4), _host(v, "v", ndim=4),
+            _host(o, "o", dtype=q.dtype, ndim=4)]
+    lp = None
+    if lse is not None:
+        lp = _host(lse, "lse", dtype=torch.float32)
+        if lse.numel() != B * Hq * T:
+            raise ValueError("lse must hold B*Hq*T floats")
+    kl = None
+    if key_lens is not None:
+        kl = _host(key_lens, "key_lens", dtype=torch.int32, ndim=1)
+        if key_lens.numel() != B:
+            raise ValueError("key_lens must have B entries")
+    need = int(lib.attn_fwd_host_workspace_size(B, Hq, Hkv, T, S, D, dt))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    wp = _dev(workspace, "workspace", dtype=torch.uint8)
+    side = [None if s is None else ctypes.c_void_p(s.cuda_stream) for s in (copy_in, copy_out)]
+    rc = lib.attn_fwd_host(*ptrs, lp, B, Hq, Hkv, T, S, D, dt, int(bool(causal)), kl,
+                           float(scale), wp, workspace.numel(), _stream(stream), *side)
+    _check(rc, "attn_fwd_host")
     return o, lse
 
 

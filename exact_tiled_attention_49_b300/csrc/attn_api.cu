@@ -14,6 +14,7 @@
 #include <mutex>
 #include <type_traits>
 #include <utility>
+#include <vector>
 
 #include "../../include/attn.h"
 #include "append.cuh"
@@ -347,6 +348,62 @@ int launch_decode_d(const attn::decode::Params& p, int G, cudaStream_t st) {
 
 bool finite_positive(float x) { return std::isfinite(x) && x > 0.f; }
 
+// The size, type and scale rules of the prefill (what fwd_dispatch checks
+// before any launch, pointers aside).
+int fwd_check_sizes(int B, int Hq, int Hkv, int T, int S, int D, int dtype, float scale) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || S <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !finite_positive(scale)) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_F16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  if (B > 65535 || Hq > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (dtype != ATTN_F32 && D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (dtype == ATTN_F32 && D > 256) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+// Device layout of attn_fwd_host's workspace: q, k, v, o, lse and key_lens
+// at 256-byte aligned offsets.
+struct HostLayout {
+  size_t q, k, v, o, lse, lens, total;
+};
+inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+HostLayout host_layout(int B, int Hq, int Hkv, int T, int S, int D, int dtype) {
+  const size_t es = dtype == ATTN_F32 ? 4 : 2;
+  const size_t nq = (size_t)B * Hq * T * D * es, nk = (size_t)B * Hkv * S * D * es;
+  HostLayout l;
+  l.q = 0;
+  l.k = align256(nq);
+  l.v = l.k + align256(nk);
+  l.o = l.v + align256(nk);
+  l.lse = l.o + align256(nq);
+  l.lens = l.lse + align256((size_t)B * Hq * T * sizeof(float));
+  l.total = l.lens + align256((size_t)B * sizeof(int32_t));
+  return l;
+}
+
+// attn_fwd_host's pipeline stages: ranges of (sequence, KV head) groups,
+// either whole sequences [b0, b0 + nb) (ng = Hkv) or KV heads [g0, g0 + ng)
+// of one sequence (nb = 1), so that each stage's q, k, v, o and lse are
+// contiguous.  About 32 MiB of inputs per stage, at most 16 stages per
+// sequence range.
+struct HostChunk {
+  int b0, nb, g0, ng;
+};
+std::vector<HostChunk> host_chunks(int B, int Hkv, size_t in_bytes) {
+  constexpr size_t kStageBytes = 32u << 20;
+  const long long units = (long long)B * Hkv;
+  const long long want = std::min<long long>(16, std::max<long long>(1, (long long)((in_bytes + kStageBytes - 1) / kStageBytes)));
+  const long long per = (units + want - 1) / want;
+  std::vector<HostChunk> out;
+  if (per >= Hkv) {
+    const int nb = (int)((per + Hkv - 1) / Hkv);
+    for (int b = 0; b < B; b += nb) out.push_back({b, std::min(nb, B - b), 0, Hkv});
+  } else {
+    for (int b = 0; b < B; ++b)
+      for (int g = 0; g < Hkv; g += (int)per) out.push_back({b, 1, g, std::min((int)per, Hkv - g)});
+  }
+  return out;
+}
+
 // Shared by attn_fwd, attn_fwd_chunked and attn_fwd_kv_shard: validation and
 // kernel choice.  `shard`: key_lens and q_pos are global positions and the
 // keys start at global position k_off (common.cuh, seq_geom).
@@ -420,6 +477,105 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              float scale, attn_stream_t stream) {
   return fwd_dispatch(q, k, v, o, lse, B, Hq, Hkv, T, S, D, dtype, causal, key_lens, nullptr,
                       scale, stream);
+}
+
+size_t attn_fwd_host_workspace_size(int B, int Hq, int Hkv, int T, int S, int D, int dtype) {
+  if (fwd_check_sizes(B, Hq, Hkv, T, S, D, dtype, 1.f) != ATTN_OK) return 0;
+  return host_layout(B, Hq, Hkv, T, S, D, dtype).total;
+}
+
+int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                  int Hkv, int T, int S, int D, int dtype, int causal, const int32_t* key_lens,
+                  float scale, void* workspace, size_t ws_bytes, attn_stream_t stream,
+                  attn_stream_t copy_in, attn_stream_t copy_out) {
+  if (!q || !k || !v || !o) return ATTN_ERR_INVALID_ARG;
+  const int rc0 = fwd_check_sizes(B, Hq, Hkv, T, S, D, dtype, scale);
+  if (rc0 != ATTN_OK) return rc0;
+  const HostLayout lay = host_layout(B, Hq, Hkv, T, S, D, dtype);
+  if (workspace == nullptr || ws_bytes < lay.total || !aligned16(workspace))
+    return ATTN_ERR_WORKSPACE;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t cin = copy_in ? reinterpret_cast<cudaStream_t>(copy_in) : st;
+  cudaStream_t cout = copy_out ? reinterpret_cast<cudaStream_t>(copy_out) : st;
+  char* ws = static_cast<char*>(workspace);
+  char *dq = ws + lay.q, *dk = ws + lay.k, *dv = ws + lay.v, *dout = ws + lay.o;
+  float* dlse = reinterpret_cast<float*>(ws + lay.lse);
+  int32_t* dlens = key_lens != nullptr ? reinterpret_cast<int32_t*>(ws + lay.lens) : nullptr;
+  const size_t es = dtype == ATTN_F32 ? 4 : 2;
+  const int G = Hq / Hkv;
+  const size_t in_bytes = lay.k + 2 * (lay.v - lay.k);
+  const std::vector<HostChunk> chunks = host_chunks(B, Hkv, in_bytes);
+  const int n = (int)chunks.size();
+
+  // Events: fork, one "inputs in" and one "computed" per chunk, join.
+  std::vector<cudaEvent_t> ev(2 * n + 2, nullptr);
+  auto release = [&]() {
+    for (cudaEvent_t e : ev)
+      if (e != nullptr) cudaEventDestroy(e);  // freed once the event completes
+  };
+  for (auto& e : ev)
+    if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) {
+      e = nullptr;
+      release();
+      return ATTN_ERR_CUDA;
+    }
+  cudaEvent_t fork = ev[0], join = ev[2 * n + 1];
+  auto ev_in = [&](int c) { return ev[1 + c]; };
+  auto ev_done = [&](int c) { return ev[1 + n + c]; };
+  bool ok = cudaEventRecord(fork, st) == cudaSuccess &&
+            cudaStreamWaitEvent(cin, fork, 0) == cudaSuccess &&
+            cudaStreamWaitEvent(cout, fork, 0) == cudaSuccess;
+  if (ok && dlens != nullptr)
+    ok = cudaMemcpyAsync(dlens, key_lens, (size_t)B * sizeof(int32_t), cudaMemcpyHostToDevice,
+                         cin) == cudaSuccess;
+  // Byte offsets of a chunk in the [B, H, rows, D] layouts.
+  auto q_off = [&](const HostChunk& c) { return ((size_t)c.b0 * Hq + (size_t)c.g0 * G) * T * D * es; };
+  auto q_len = [&](const HostChunk& c) { return (size_t)c.nb * c.ng * G * T * D * es; };
+  auto k_off = [&](const HostChunk& c) { return ((size_t)c.b0 * Hkv + c.g0) * S * D * es; };
+  auto k_len = [&](const HostChunk& c) { return (size_t)c.nb * c.ng * S * D * es; };
+  auto l_off = [&](const HostChunk& c) { return ((size_t)c.b0 * Hq + (size_t)c.g0 * G) * T; };
+  auto l_len = [&](const HostChunk& c) { return (size_t)c.nb * c.ng * G * T; };
+  // Enqueued phase by phase (all copies in, all launches, all copies out),
+  // so that a copy to pageable host memory, which returns only when it is
+  // done, cannot hold back the enqueueing of the other chunks.
+  for (int c = 0; ok && c < n; ++c) {
+    const HostChunk& ch = chunks[c];
+    ok = cudaMemcpyAsync(dq + q_off(ch), static_cast<const char*>(q) + q_off(ch), q_len(ch),
+                         cudaMemcpyHostToDevice, cin) == cudaSuccess &&
+         cudaMemcpyAsync(dk + k_off(ch), static_cast<const char*>(k) + k_off(ch), k_len(ch),
+                         cudaMemcpyHostToDevice, cin) == cudaSuccess &&
+         cudaMemcpyAsync(dv + k_off(ch), static_cast<const char*>(v) + k_off(ch), k_len(ch),
+                         cudaMemcpyHostToDevice, cin) == cudaSuccess &&
+         cudaEventRecord(ev_in(c), cin) == cudaSuccess;
+  }
+  int rc = ok ? ATTN_OK : ATTN_ERR_CUDA;
+  for (int c = 0; rc == ATTN_OK && c < n; ++c) {
+    const HostChunk& ch = chunks[c];
+    if (cudaStreamWaitEvent(st, ev_in(c), 0) != cudaSuccess) {
+      rc = ATTN_ERR_CUDA;
+      break;
+    }
+    rc = fwd_dispatch(dq + q_off(ch), dk + k_off(ch), dv + k_off(ch), dout + q_off(ch),
+                      lse != nullptr ? dlse + l_off(ch) : nullptr, ch.nb, ch.ng * G, ch.ng, T, S,
+                      D, dtype, causal, dlens != nullptr ? dlens + ch.b0 : nullptr, nullptr, scale,
+                      stream);
+    if (rc == ATTN_OK && cudaEventRecord(ev_done(c), st) != cudaSuccess) rc = ATTN_ERR_CUDA;
+  }
+  for (int c = 0; rc == ATTN_OK && c < n; ++c) {
+    const HostChunk& ch = chunks[c];
+    if (cudaStreamWaitEvent(cout, ev_done(c), 0) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<char*>(o) + q_off(ch), dout + q_off(ch), q_len(ch),
+                        cudaMemcpyDeviceToHost, cout) != cudaSuccess ||
+        (lse != nullptr &&
+         cudaMemcpyAsync(lse + l_off(ch), dlse + l_off(ch), l_len(ch) * sizeof(float),
+                         cudaMemcpyDeviceToHost, cout) != cudaSuccess))
+      rc = ATTN_ERR_CUDA;
+  }
+  // Join: work enqueued on `stream` after this call follows the last copy out.
+  if (cudaEventRecord(join, cout) != cudaSuccess || cudaStreamWaitEvent(st, join, 0) != cudaSuccess)
+    rc = ATTN_ERR_CUDA;
+  release();
+  return rc;
 }
 
 int attn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,

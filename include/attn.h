@@ -8,8 +8,9 @@
  * Conventions shared by every entry point
  * ----------------------------------------
  *  - All tensor arguments are DEVICE pointers to contiguous row-major arrays
- *    that the caller allocates, owns and frees.  The library keeps no
- *    per-call state and allocates no device memory on these paths.
+ *    that the caller allocates, owns and frees (attn_fwd_host alone takes
+ *    host arrays).  The library keeps no per-call state and allocates no
+ *    device memory on these paths.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *    default stream).  A non-zero return means nothing was launched, except
  *    ATTN_ERR_CUDA, which reports a launch error seen right after launching.
@@ -99,6 +100,62 @@ ATTN_API int attn_fwd(const void* q, const void* k, const void* v, void* o, floa
              int B, int Hq, int Hkv, int T, int S, int D, int dtype,
              int causal, const int32_t* key_lens, float scale,
              attn_stream_t stream);
+
+/*
+ * attn_fwd_host_workspace_size -- bytes of device memory attn_fwd_host needs
+ * for these sizes: device copies of q, k, v, o, lse and key_lens, each at a
+ * 256-byte aligned offset.  Returns 0 for invalid or unsupported sizes.
+ */
+ATTN_API size_t attn_fwd_host_workspace_size(int B, int Hq, int Hkv, int T, int S, int D,
+                                             int dtype);
+
+/*
+ * attn_fwd_host -- attn_fwd on HOST buffers: copies q, k, v (and key_lens)
+ * to the device, computes exactly what attn_fwd computes (same kernels,
+ * bit-identical results), and copies o (and lse) back.  The computation is
+ * the one attn_fwd cites; the pages have no counterpart for the copies,
+ * which exist because a caller's tensors may live in host memory.
+ *
+ * The work is cut into stages along (sequence, KV head group) -- whole
+ * sequences, or KV heads of one sequence, about 32 MiB of inputs each --
+ * and pipelined over three streams: stage c's inputs are copied in on
+ * copy_in while stage c-1 computes on `stream` and stage c-2's results are
+ * copied out on copy_out, so a large call costs about its host-to-device
+ * copy time rather than the sum of copies and compute.  Every operation is
+ * ordered after the work already enqueued on `stream`, and work enqueued on
+ * `stream` after this call is ordered after the last copy out (events; the
+ * call is capturable in a CUDA graph).
+ *
+ *   q                 [B,Hq,T,D]   dtype, HOST     (read)
+ *   k, v              [B,Hkv,S,D]  dtype, HOST     (read)
+ *   o                 [B,Hq,T,D]   dtype, HOST     (written)
+ *   lse               [B,Hq,T]     float32, HOST   (written; NULL = do not emit)
+ *   key_lens          [B]          int32, HOST     (NULL = every key valid;
+ *                                                   clamped to [0, S] as in
+ *                                                   attn_fwd)
+ *   workspace         device, >= attn_fwd_host_workspace_size(...) bytes,
+ *                     16-byte aligned; owned by the caller, its contents on
+ *                     entry do not matter; the device copies of the inputs
+ *                     and results stay in it after the call
+ *   stream            runs the kernels (and every copy when copy_in /
+ *                     copy_out are NULL)
+ *   copy_in, copy_out streams for the host-to-device and device-to-host
+ *                     copies (NULL = `stream`, no overlap for that role)
+ *
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister):
+ * copies from or to pageable memory are correct but staged by the driver
+ * and do not overlap.  All host buffers must stay valid, and the inputs
+ * unmodified, until `stream` has completed the call's work.  Sizes, types
+ * and masks as for attn_fwd.  Returns ATTN_OK, ATTN_ERR_INVALID_ARG,
+ * ATTN_ERR_UNSUPPORTED or ATTN_ERR_WORKSPACE with nothing enqueued, or
+ * ATTN_ERR_CUDA if a copy, event or launch failed (part of the work may then
+ * have been enqueued).
+ */
+ATTN_API int attn_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int Hq, int Hkv, int T, int S, int D, int dtype, int causal,
+                           const int32_t* key_lens, float scale, void* workspace,
+                           size_t ws_bytes, attn_stream_t stream, attn_stream_t copy_in,
+                           attn_stream_t copy_out);
 
 /*
  * attn_fwd_fp8 -- attn_fwd on FP8 E4M3 inputs ("Self-Attention:

@@ -201,3 +201,28 @@ def test_kv_shard_and_merge_reject_bad_arguments(lib):
     assert mg(dt=9) == 1
     assert mg(D=4) == 2                    # 8-byte rows cannot be merged as 16-byte vectors
     assert mg(o=MIS) == 1
+
+
+def test_fwd_host_workspace_and_rejections(lib):
+    # q, k, v, o, lse and key_lens at 256-byte aligned offsets
+    a = lambda x: (x + 255) // 256 * 256
+    B, Hq, Hkv, T, S, D = 3, 8, 2, 100, 130, 64
+    want = 2 * a(B * Hq * T * D * 2) + 2 * a(B * Hkv * S * D * 2) + a(B * Hq * T * 4) + a(B * 4)
+    assert lib.attn_fwd_host_workspace_size(B, Hq, Hkv, T, S, D, 1) == want
+    assert lib.attn_fwd_host_workspace_size(B, Hq, Hkv, T, S, D, 0) == \
+        2 * a(B * Hq * T * D * 4) + 2 * a(B * Hkv * S * D * 4) + a(B * Hq * T * 4) + a(B * 4)
+    assert lib.attn_fwd_host_workspace_size(0, 1, 1, 8, 8, 64, 1) == 0
+    assert lib.attn_fwd_host_workspace_size(1, 1, 1, 8, 8, 96, 1) == 0   # unsupported D
+    need = lib.attn_fwd_host_workspace_size(1, 2, 1, 8, 8, 64, 1)
+
+    def fh(q=FAKE, ws=FAKE, ws_bytes=need, D=64, dt=1, Hq=2, Hkv=1, scale=0.125):
+        return lib.attn_fwd_host(q, FAKE, FAKE, FAKE, None, 1, Hq, Hkv, 8, 8, D, dt, 1, None,
+                                 scale, ws, ws_bytes, None, None, None)
+    assert fh(q=None) == 1
+    assert fh(Hq=3, Hkv=2) == 1
+    assert fh(scale=-1.0) == 1
+    assert fh(dt=5) == 1
+    assert fh(D=96) == 2
+    assert fh(ws=None) == 3
+    assert fh(ws_bytes=need - 1) == 3
+    assert fh(ws=MIS) == 3
