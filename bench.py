@@ -12,14 +12,18 @@ figure and CPU baseline: the metric names both halves.  ``--workload 2``
 times the short causal prefill plus the next-token append and decode of the
 same batch; ``--workload 5`` the padded batch prefill; ``--workload 4`` the
 decode step alone.  Inputs are seeded synthetic tensors already resident in
-HBM; L2 is flushed (256 MiB write) between timed steps, outside the timed
-events.
+HBM; L2 is flushed (256 MiB write) between timed prefill steps, outside the
+timed events; the decode steps, which each read a 1.3 GB cache (ten times
+L2), are timed back to back in one CUDA graph, and the flushed per-step
+figure is reported beside them.
 
 Printed: ONE JSON line (rank 0) with the metric, whole-job throughput, the
 roofline of the dominant kernel (its own CUDA-event time), an end-to-end
-figure through the public API with host buffers (with its copy / call
-breakdown), the float64 CPU oracle timed on the host cores, SM clocks sampled
-during the timed region and the number of library kernels launched.
+figure through the public API with host buffers (the prefill through
+attn_fwd_host, whose copies overlap the compute; the serial copy / call
+breakdown beside it), the float64 CPU oracle timed on the host cores, SM
+clocks sampled during the timed region and the number of library kernels
+launched.
 
 ``--impl reference`` times the float64 CPU oracle (the reference arm; there
 is no installable reference implementation) on bounded samples of the same
@@ -172,6 +176,17 @@ class _NvmlCtypes:
     def nvmlDeviceGetClockInfo(self, h, typ):
         return self._clock(self.lib.nvmlDeviceGetClockInfo, h, typ)
 
+    def _uint(self, fn, h):
+        v = self.ct.c_uint()
+        self._chk(fn(h, self.ct.byref(v)))
+        return v.value
+
+    def nvmlDeviceGetPowerUsage(self, h):
+        return self._uint(self.lib.nvmlDeviceGetPowerUsage, h)
+
+    def nvmlDeviceGetEnforcedPowerLimit(self, h):
+        return self._uint(self.lib.nvmlDeviceGetEnforcedPowerLimit, h)
+
     def nvmlDeviceGetCurrentClocksEventReasons(self, h):
         v = self.ct.c_ulonglong()
         fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
@@ -187,14 +202,18 @@ class ClockSampler:
     at exit; if NVML is unavailable, nvidia-smi queries instead."""
 
     REASONS = {
+        "gpu_idle": 0x1, "applications_clocks_setting": 0x2,
         "sw_power_cap": 0x4, "hw_slowdown": 0x8, "sync_boost": 0x10,
         "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
-        "hw_power_brake_slowdown": 0x80,
+        "hw_power_brake_slowdown": 0x80, "display_clock_setting": 0x100,
     }
 
     def __init__(self, device, period_s: float = 0.002):
         self.period = period_s
         self.samples, self.reasons = [], set()
+        self.power_w = []
+        self.limit_w = None
+        self.mask = 0
         self.max_mhz = None
         self.error = None
         self._stop = threading.Event()
@@ -221,6 +240,10 @@ class ClockSampler:
             self._reasons_fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
                 getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
             self.mode = "nvml" if not isinstance(pynvml, _NvmlCtypes) else "nvml-ctypes"
+            try:
+                self.limit_w = pynvml.nvmlDeviceGetEnforcedPowerLimit(self.h) / 1000.0
+            except Exception:
+                self.limit_w = None
         except Exception as e:  # fall back to nvidia-smi
             self.error = f"nvml: {type(e).__name__}: {e}"
             self.mode = "smi"
@@ -228,9 +251,14 @@ class ClockSampler:
     def _sample_nvml(self):
         self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
         mask = self._reasons_fn(self.h)
+        self.mask |= int(mask)
         for name, bit in self.REASONS.items():
             if mask & bit:
                 self.reasons.add(name)
+        try:
+            self.power_w.append(self.nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0)
+        except Exception:
+            pass
 
     def _sample_smi(self):
         import subprocess
@@ -272,6 +300,14 @@ class ClockSampler:
         rec = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
                "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
                "samples": len(self.samples), "source": self.mode}
+        if self.mode != "smi":
+            rec["reasons_mask"] = hex(self.mask)  # union of NVML's clock-event bits
+        if self.power_w:
+            # NVML's board power is a trailing average (about a second): it
+            # lags a short timed region
+            rec["power_w_trailing_avg"] = statistics.median(self.power_w)
+        if self.limit_w:
+            rec["power_limit_w"] = self.limit_w
         if self.error:
             rec["error"] = self.error
         return rec
@@ -502,6 +538,55 @@ def time_graphs(E, c, steps, flush, clk=None, sync=None):
     kern_ms = {name: sum(ev[i].elapsed_time(ev[i + 1]) for ev in events) / steps
                for i, (name, _) in enumerate(graphs)}
     return step_ms, kern_ms, launches_per_step
+
+
+def time_stream(E, c, steps, clk=None, sync=None):
+    """`steps` steps back to back in one CUDA graph, without an L2 flush
+    between them: for the decode step, whose input (the KV cache, 1.3 GB)
+    is ten times the L2, so every step reads it from DRAM anyway.  A serving
+    loop issues its steps back to back, and so does this timing: each call's
+    launch overlaps the previous call's tail (PDL) instead of being timed
+    alone.  Returns (ms for all the steps, ms per decode call from a second
+    graph of `steps` decode calls, library launches per step)."""
+    import torch
+    groups = step_groups(c)
+    n0 = E.attn_kernel_launches()
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        for _ in range(steps):
+            for _, fn in groups:
+                fn()
+    launches = (E.attn_kernel_launches() - n0) // steps
+    dec = [fn for name, fn in groups if name == "decode"][0]
+    g_dec = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_dec):
+        for _ in range(steps):
+            dec()
+    for _ in range(2):
+        g_step.replay()
+        g_dec.replay()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    if sync is not None:
+        sync()
+    torch.cuda.synchronize()
+    if clk is not None:
+        clk.__enter__()
+    try:
+        ev[0].record()
+        g_step.replay()
+        ev[1].record()
+        torch.cuda.synchronize()
+    finally:
+        if clk is not None:
+            clk.__exit__(None, None, None)
+    if sync is not None:
+        sync()
+    ev[2].record()
+    g_dec.replay()
+    ev[3].record()
+    torch.cuda.synchronize()
+    return ev[0].elapsed_time(ev[1]), ev[2].elapsed_time(ev[3]) / steps, launches
 
 
 def other_workloads(E, skip, device, steps, peaks):
@@ -874,8 +959,10 @@ def cpu_baseline_bwd(wid, budget_s=12.0, seed=0):
 def measure_block(E, args, wid, device, peaks, ws, rank, backward=False, fp8=False,
                   batch=None):
     """One workload measured for the JSON line: warm-up steps, K timed steps
-    (CUDA-graph replays, L2 flushed between steps, clocks sampled, barrier and
-    max over ranks), the roofline of its dominant kernel, the end-to-end
+    (CUDA-graph replays, L2 flushed between steps -- for the decode step, whose
+    cache is far larger than L2, the K steps back to back in one graph, with
+    the flushed per-step timing reported beside it -- clocks sampled, barrier
+    and max over ranks), the roofline of its dominant kernel, the end-to-end
     figure through the public API, and (rank 0) the float64 oracle timed on
     the host cores.  Returns the block's dict."""
     import torch
@@ -891,9 +978,23 @@ def measure_block(E, args, wid, device, peaks, ws, rank, backward=False, fp8=Fal
 
     K = args.steps
     clk = ClockSampler(device)
-    step_ms, kern_ms, launches_per_step = time_graphs(E, c, K, flush, clk,
-                                                      sync=lambda: barrier(ws))
-    total_ms = reduce_max(sum(step_ms), ws, device)
+    isolated = None
+    if w.kind == "decode":
+        # each step alone after an L2 flush (reported), then the K steps back
+        # to back (the value): the cache is far larger than L2
+        step_ms, kern_ms, launches_per_step = time_graphs(E, c, K, flush, ClockSampler(device))
+        isolated = {"ms_per_step": sum(step_ms) / K, "decode_ms": kern_ms["decode"],
+                    "append_ms": kern_ms["append"],
+                    "value": c["dec_bytes"] / (sum(step_ms) / K * 1e-3) / 1e9,
+                    "timing": "each step alone: L2 flushed before it, CUDA events around "
+                              "its graph replays"}
+        tot_ms, dec_ms, launches_per_step = time_stream(E, c, K, clk, sync=lambda: barrier(ws))
+        total_ms = reduce_max(tot_ms, ws, device)
+        kern_ms = {"decode": dec_ms, "append": kern_ms["append"]}
+    else:
+        step_ms, kern_ms, launches_per_step = time_graphs(E, c, K, flush, clk,
+                                                          sync=lambda: barrier(ws))
+        total_ms = reduce_max(sum(step_ms), ws, device)
     if E.attn_device_error(clear=True) != 0:
         raise RuntimeError("device error during the timed region")
     ms_per_step = total_ms / K
@@ -936,6 +1037,7 @@ def measure_block(E, args, wid, device, peaks, ws, rank, backward=False, fp8=Fal
                            "traffic": profiled_traffic(wid) if batch is None else None,
                            "peak_source": peaks["source"] + " HBM copy",
                            "kernel_ms": kern_ms["decode"], "append_ms": kern_ms["append"]}
+        out["isolated_step"] = isolated
     cfg = {"workload": ("backward (dQ, dK, dV, 2.5x the forward's FLOPs) of: " + w.name
                         if "bwd" in c else
                         "E4M3 inputs (per-tensor descales): " + w.name if "fp8" in c else w.name),
@@ -951,10 +1053,31 @@ def measure_block(E, args, wid, device, peaks, ws, rank, backward=False, fp8=Fal
             cfg["q_scale"] = w.q_scale
     else:
         cfg.update({"cache_len": f"U[{w.lens[0]},{w.lens[1]}]", "S_max": c["S_max"],
-                    "kv_bytes_per_step": c["dec_bytes"]})
+                    "kv_bytes_per_step": c["dec_bytes"],
+                    "l2": "not flushed: the K steps run back to back and each reads "
+                          f"{c['dec_bytes'] / 1e9:.2f} GB of K/V, ten times the 126 MB L2 "
+                          "(isolated_step: flushed)",
+                    "timing": "CUDA events around one CUDA graph of the K steps back to back; "
+                              "roofline: a graph of K decode calls"})
     out["config"] = cfg
     out["gpu_launches"] = int(launches_per_step * K)
     out["clocks"] = clk.record()
+    if out["roofline"]["bound"] == "tensor":
+        # The burst peak was measured at full clocks; a prefill timed over
+        # many steps runs into the 1100 W cap (sw_power_cap, ~1.46 GHz for
+        # the long-context kernel), the regime of the sustained peak.  Also
+        # the fraction of the tensor rate at the SM clock actually sampled:
+        # 8192 dense 16-bit FLOP per cycle per SM (M128 N128 K16 in 64
+        # cycles), twice that for E4M3.
+        r = out["roofline"]
+        f8 = 2.0 if "fp8" in c else 1.0
+        r["peak_sustained"] = peaks["bf16_tflops_sustained"] * f8
+        r["frac_sustained"] = r["achieved"] / r["peak_sustained"]
+        mhz = out["clocks"].get("sm_mhz")
+        if mhz:
+            sms = torch.cuda.get_device_properties(device).multi_processor_count
+            r["peak_at_sampled_clock"] = 8192.0 * f8 * sms * mhz * 1e6 / 1e12
+            r["frac_at_sampled_clock"] = r["achieved"] / r["peak_at_sampled_clock"]
 
     if not args.no_e2e:
         # End to end through the public API with host buffers.  A plain
