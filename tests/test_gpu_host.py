@@ -59,6 +59,8 @@ CASES = [
     (torch.bfloat16, 8, 4, 4, 2048, 2048, 128, True,
      [2048, 1500, 2047, 1, 777, 2048, 1024, 0], True, True, True),                   # stages of sequences
     (torch.bfloat16, 2, 32, 8, 1024, 3072, 64, False, [3072, 2000], True, True, False),
+    (torch.bfloat16, 1, 32, 8, 8192, 8192, 128, True, [8000], True, True, True),      # GQA, 3 stages of KV heads
+    (torch.bfloat16, 2, 16, 16, 4096, 4096, 128, True, [4096, 3000], True, True, True),  # 2 stages per sequence
     (torch.float16, 2, 8, 8, 2000, 2000, 128, True, [2000, 1999], True, False, True),  # copies on the compute stream
     (torch.float32, 2, 4, 2, 96, 160, 64, True, [160, 90], False, True, True),        # pageable host memory
 ]
@@ -126,3 +128,36 @@ def test_host_orders_after_and_before_stream_work(E):
     st.synchronize()
     o_dev, _ = E.attn_fwd(q, k, v, causal=True)
     assert torch.equal(back.view(torch.int16), o_dev.view(torch.int16))
+
+
+def test_host_call_captures_in_a_graph(E):
+    """The call forks to its copy streams and joins back with events, so it
+    can be captured in a CUDA graph; replays recompute from the host inputs."""
+    B, Hq, Hkv, T, S, D = 1, 16, 16, 4096, 4096, 128   # two stages
+    q, k, v, _ = _inputs(B, Hq, Hkv, T, S, D, torch.bfloat16, seed=13)
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    o_h = torch.zeros(q.shape, dtype=torch.bfloat16, pin_memory=True)
+    lse_h = torch.zeros((B, Hq, T), pin_memory=True)
+    ws = torch.empty(E.attn_fwd_host_workspace_size(B, Hq, Hkv, T, S, D, torch.bfloat16),
+                     dtype=torch.uint8, device="cuda")
+    cin, cout = torch.cuda.Stream(), torch.cuda.Stream()
+    E.attn_fwd_host(hq, hk, hv, o=o_h, lse=lse_h, causal=True, workspace=ws, copy_in=cin,
+                    copy_out=cout)     # warm (tensor maps, kernel attributes)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        E.attn_fwd_host(hq, hk, hv, o=o_h, lse=lse_h, causal=True, workspace=ws,
+                        copy_in=cin, copy_out=cout)
+    o_h.zero_()
+    lse_h.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    o_dev, lse_dev = E.attn_fwd(q, k, v, causal=True)
+    assert torch.equal(o_h.view(torch.int16), o_dev.cpu().view(torch.int16))
+    assert torch.equal(lse_h.view(torch.int32), lse_dev.cpu().view(torch.int32))
+    # new host inputs, same graph: the replay reads them
+    hq.copy_(torch.flip(hq, dims=[2]))
+    g.replay()
+    torch.cuda.synchronize()
+    o_dev2, _ = E.attn_fwd(hq.cuda(), k, v, causal=True)
+    assert torch.equal(o_h.view(torch.int16), o_dev2.cpu().view(torch.int16))
