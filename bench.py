@@ -81,9 +81,10 @@ PROFILED_TRAFFIC = {
     5: {"source": "exact_tiled_attention_49_b300/csrc/fwd_bf16_tc.cuh", "sha256": "103911b9e59f",
         "bytes": 1082.855168e6 + 90.0608e6, "scale": 1.0,
         "capture": "fwd_bf16_tc_kernel<128,0,0>, full workload"},
-    4: {"source": "exact_tiled_attention_49_b300/csrc/decode.cuh", "sha256": "15c773026e9f",
-        "bytes": 1339.576576e6 + 4.541696e6 + 3.42272e6, "scale": 1.0,
-        "capture": "decode_split_mma_kernel<128,4,0> + decode_combine_spans_kernel, full workload"},
+    4: {"source": "exact_tiled_attention_49_b300/csrc/decode.cuh", "sha256": "b48fe69c4059",
+        "bytes": 1339.883776e6 + 4.811776e6 + 3.421952e6, "scale": 1.0,
+        "capture": "decode_split_mma_kernel<128,4,0> (append fused) + "
+                   "decode_combine_spans_kernel, full workload"},
 }
 
 
@@ -453,19 +454,15 @@ def step_groups(c):
         if "dec" in c:
             d = c["dec"]
 
-            def dec():
-                E.kv_cache_append(d["kcache"], d["vcache"], d["k_new"], d["v_new"], d["pos"])
-                E.attn_decode(d["q"], d["kcache"], d["vcache"], d["kv_len"], o=d["o"],
-                              lse=d["lse"], workspace=d["ws"], scale=scale)
-            groups.append(("decode", dec))
+            groups.append(("decode", lambda: E.attn_decode_append(
+                d["q"], d["kcache"], d["vcache"], d["k_new"], d["v_new"], d["kv_len"], o=d["o"],
+                lse=d["lse"], workspace=d["ws"], scale=scale)))
     else:
-        # the decode step: append the new token, then decode (split + combine);
-        # two groups so that the decode call has its own time
-        groups.append(("append", lambda: E.kv_cache_append(
-            c["kcache"], c["vcache"], c["k_new"], c["v_new"], c["cache_len"])))
-        groups.append(("decode", lambda: E.attn_decode(
-            c["q"], c["kcache"], c["vcache"], c["kv_len"], o=c["o"], lse=c["lse"],
-            workspace=c["ws"], scale=scale)))
+        # the decode step: append the new token and decode over the cache
+        # including it, in one call (split kernel + merge)
+        groups.append(("decode", lambda: E.attn_decode_append(
+            c["q"], c["kcache"], c["vcache"], c["k_new"], c["v_new"], c["kv_len"], o=c["o"],
+            lse=c["lse"], workspace=c["ws"], scale=scale)))
     return groups
 
 
@@ -546,8 +543,8 @@ def time_stream(E, c, steps, clk=None, sync=None):
     is ten times the L2, so every step reads it from DRAM anyway.  A serving
     loop issues its steps back to back, and so does this timing: each call's
     launch overlaps the previous call's tail (PDL) instead of being timed
-    alone.  Returns (ms for all the steps, ms per decode call from a second
-    graph of `steps` decode calls, library launches per step)."""
+    alone.  Returns (ms for all the steps, ms per step, library launches
+    per step)."""
     import torch
     groups = step_groups(c)
     n0 = E.attn_kernel_launches()
@@ -557,16 +554,10 @@ def time_stream(E, c, steps, clk=None, sync=None):
             for _, fn in groups:
                 fn()
     launches = (E.attn_kernel_launches() - n0) // steps
-    dec = [fn for name, fn in groups if name == "decode"][0]
-    g_dec = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_dec):
-        for _ in range(steps):
-            dec()
     for _ in range(2):
         g_step.replay()
-        g_dec.replay()
     torch.cuda.synchronize()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     if sync is not None:
         sync()
     torch.cuda.synchronize()
@@ -582,11 +573,8 @@ def time_stream(E, c, steps, clk=None, sync=None):
             clk.__exit__(None, None, None)
     if sync is not None:
         sync()
-    ev[2].record()
-    g_dec.replay()
-    ev[3].record()
-    torch.cuda.synchronize()
-    return ev[0].elapsed_time(ev[1]), ev[2].elapsed_time(ev[3]) / steps, launches
+    ms = ev[0].elapsed_time(ev[1])
+    return ms, ms / steps, launches
 
 
 def other_workloads(E, skip, device, steps, peaks):
@@ -619,13 +607,15 @@ def other_workloads(E, skip, device, steps, peaks):
                 gbs = c["dec_bytes"] / (kern_ms["decode"] * 1e-3) / 1e9
                 out[str(wid)]["next_token_decode"] = {
                     "value": gbs, "unit": "GB/s", "ms": kern_ms["decode"],
-                    "kernels": "kv_append_kernel, decode_split_mma_kernel, decode_combine_kernel",
+                    "kernels": "decode_split_mma_kernel (append fused), "
+                               "decode_combine_spans_kernel",
                     "frac": gbs / peaks["hbm_gbs"]}
         else:
             v = c["dec_bytes"] / (kern_ms["decode"] * 1e-3) / 1e9
             out[str(wid)] = {"workload": w.name, "value": v, "unit": "GB/s",
-                             "ms": kern_ms["decode"], "append_ms": kern_ms["append"],
-                             "kernel": "decode_split_mma_kernel+decode_combine_kernel",
+                             "ms": kern_ms["decode"],
+                             "kernel": "decode_split_mma_kernel (append fused)"
+                                       "+decode_combine_spans_kernel",
                              "frac": v / peaks["hbm_gbs"], "traffic": profiled_traffic(wid),
                              "clocks": clk.record()}
         del c
@@ -983,14 +973,13 @@ def measure_block(E, args, wid, device, peaks, ws, rank, backward=False, fp8=Fal
         # each step alone after an L2 flush (reported), then the K steps back
         # to back (the value): the cache is far larger than L2
         step_ms, kern_ms, launches_per_step = time_graphs(E, c, K, flush, ClockSampler(device))
-        isolated = {"ms_per_step": sum(step_ms) / K, "decode_ms": kern_ms["decode"],
-                    "append_ms": kern_ms["append"],
+        isolated = {"ms_per_step": sum(step_ms) / K,
                     "value": c["dec_bytes"] / (sum(step_ms) / K * 1e-3) / 1e9,
                     "timing": "each step alone: L2 flushed before it, CUDA events around "
                               "its graph replays"}
         tot_ms, dec_ms, launches_per_step = time_stream(E, c, K, clk, sync=lambda: barrier(ws))
         total_ms = reduce_max(tot_ms, ws, device)
-        kern_ms = {"decode": dec_ms, "append": kern_ms["append"]}
+        kern_ms = {"decode": dec_ms}
     else:
         step_ms, kern_ms, launches_per_step = time_graphs(E, c, K, flush, clk,
                                                           sync=lambda: barrier(ws))
@@ -1031,12 +1020,13 @@ def measure_block(E, args, wid, device, peaks, ws, rank, backward=False, fp8=Fal
         out["value"] = c["dec_bytes"] * ws / (ms_per_step * 1e-3) / 1e9
         out["unit"] = "GB/s"
         achieved = c["dec_bytes"] / (kern_ms["decode"] * 1e-3) / 1e9
-        out["roofline"] = {"kernel": "decode_split_mma_kernel+decode_combine_kernel",
+        out["roofline"] = {"kernel": "decode_split_mma_kernel (new token's K/V written in it)"
+                                     "+decode_combine_spans_kernel",
                            "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
                            "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                            "traffic": profiled_traffic(wid) if batch is None else None,
                            "peak_source": peaks["source"] + " HBM copy",
-                           "kernel_ms": kern_ms["decode"], "append_ms": kern_ms["append"]}
+                           "kernel_ms": kern_ms["decode"]}
         out["isolated_step"] = isolated
     cfg = {"workload": ("backward (dQ, dK, dV, 2.5x the forward's FLOPs) of: " + w.name
                         if "bwd" in c else
@@ -1057,8 +1047,8 @@ def measure_block(E, args, wid, device, peaks, ws, rank, backward=False, fp8=Fal
                     "l2": "not flushed: the K steps run back to back and each reads "
                           f"{c['dec_bytes'] / 1e9:.2f} GB of K/V, ten times the 126 MB L2 "
                           "(isolated_step: flushed)",
-                    "timing": "CUDA events around one CUDA graph of the K steps back to back; "
-                              "roofline: a graph of K decode calls"})
+                    "timing": "CUDA events around one CUDA graph of the K steps back to back "
+                              "(each step one attn_decode_append call: append + decode)"})
     out["config"] = cfg
     out["gpu_launches"] = int(launches_per_step * K)
     out["clocks"] = clk.record()

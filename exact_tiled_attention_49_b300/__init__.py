@@ -11,6 +11,7 @@ ABI (``include/attn.h``); this package is a thin ctypes binding of it.
 from ._lib import (ATTN_BF16, ATTN_ERR_CUDA, ATTN_F16, ATTN_ERR_INVALID_ARG,  # noqa: F401
                    ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE, ATTN_F32, ATTN_OK,
                    LIB_PATH, NOALLOC_SCRATCH_BYTES, SIGNATURES, AttnError, attn_decode,
+                   attn_decode_append,
                    attn_decode_noalloc,
                    attn_bwd, attn_bwd_workspace_size,
                    attn_decode_workspace_size, attn_device_error, attn_fwd, attn_fwd_chunked,
@@ -21,7 +22,7 @@ from ._lib import (ATTN_BF16, ATTN_ERR_CUDA, ATTN_F16, ATTN_ERR_INVALID_ARG,  # 
                    status_string)
 
 __all__ = [
-    "attn_fwd", "attn_fwd_host", "attn_fwd_host_workspace_size", "attn_fwd_chunked", "attn_fwd_fp8", "attn_fwd_kv_shard", "attn_lse_merge", "attn_bwd", "attn_bwd_workspace_size", "attn_decode", "attn_decode_workspace_size", "attn_decode_noalloc",
+    "attn_fwd", "attn_fwd_host", "attn_fwd_host_workspace_size", "attn_fwd_chunked", "attn_fwd_fp8", "attn_fwd_kv_shard", "attn_lse_merge", "attn_bwd", "attn_bwd_workspace_size", "attn_decode", "attn_decode_append", "attn_decode_workspace_size", "attn_decode_noalloc",
     "kv_cache_append",
     "attn_status_string", "attn_kernel_launches", "attn_device_error", "AttnError",
     "attn_selftest_wait_timeout", "ATTN_SELFTEST_ERROR",

@@ -39,6 +39,8 @@ SIGNATURES = {
     "attn_decode_workspace_size": (ctypes.c_size_t, [_I, _I, _I, _I]),
     "attn_decode": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
                          ctypes.c_size_t, _P]),
+    "attn_decode_append": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P,
+                                ctypes.c_size_t, _P]),
     "attn_decode_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P]),
     "kv_cache_append": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]),
     "attn_status_string": (ctypes.c_char_p, [_I]),
@@ -446,6 +448,45 @@ def attn_decode(q, kcache, vcache, kv_lens, o=None, lse=None, workspace=None,
                          float(scale), _dev(workspace, "workspace"),
                          workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "attn_decode")
+    return o, lse
+
+
+def attn_decode_append(q, kcache, vcache, k_new, v_new, kv_lens, o=None, lse=None,
+                       workspace=None, scale=None, return_lse=True, stream=None):
+    """Append the new token's K/V rows (k_new, v_new [B,Hkv,D]) at row
+    kv_lens[b] - 1 of the caches and decode over kv_lens[b] rows, in one call
+    (bf16 or fp16).  kv_lens counts the new token.  Same results as
+    kv_cache_append(pos=kv_lens - 1) followed by attn_decode.
+    Returns (o [B,Hq,D], lse [B,Hq] or None)."""
+    lib = load()
+    B, Hq, D = q.shape
+    Bk, Hkv, S_max, Dk = kcache.shape
+    if Bk != B or Dk != D or tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError("q/cache shape mismatch")
+    if tuple(k_new.shape) != (B, Hkv, D) or tuple(v_new.shape) != (B, Hkv, D):
+        raise ValueError("k_new and v_new must be [B, Hkv, D]")
+    for name, t in (("kcache", kcache), ("vcache", vcache), ("k_new", k_new), ("v_new", v_new)):
+        if t.dtype != q.dtype:
+            raise TypeError(f"{name} must have q's dtype")
+    dt = _dtype_code(q)
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq), device=q.device, dtype=torch.float32)
+    need = attn_decode_workspace_size(B, Hq, S_max, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=q.device, dtype=torch.uint8)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lp = _dev(lse, "lse", dtype=torch.float32) if lse is not None else None
+    rc = lib.attn_decode_append(_dev(q, "q", ndim=3), _dev(kcache, "kcache", ndim=4),
+                                _dev(vcache, "vcache", ndim=4), _dev(k_new, "k_new", ndim=3),
+                                _dev(v_new, "v_new", ndim=3),
+                                _dev(kv_lens, "kv_lens", dtype=torch.int32, ndim=1),
+                                _dev(o, "o", dtype=q.dtype, ndim=3), lp, B, Hq, Hkv, S_max, D, dt,
+                                float(scale), _dev(workspace, "workspace"),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "attn_decode_append")
     return o, lse
 
 

@@ -732,21 +732,24 @@ int decode_validate(const void* q, const void* kcache, const void* vcache,
   return ATTN_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-int attn_decode(const void* q, const void* kcache, const void* vcache, const int32_t* kv_lens,
-                void* o, float* lse, int B, int Hq, int Hkv, int S_max, int D, int dtype,
-                float scale, void* workspace, size_t ws_bytes, attn_stream_t stream) {
-  const int rc = decode_validate(q, kcache, vcache, kv_lens, o, lse, B, Hq, Hkv, S_max, D, dtype,
-                                 scale);
-  if (rc != ATTN_OK) return rc;
+// A validated decode step (attn_decode, attn_decode_append): the workspace
+// check and the launches.  k_new / v_new non-null: the new token's rows are
+// written into the caches by the split kernel (bf16 / fp16 only).
+int decode_run(const void* q, void* kcache, void* vcache, const int32_t* kv_lens, void* o,
+               float* lse, int B, int Hq, int Hkv, int S_max, int D, int dtype, float scale,
+               void* workspace, size_t ws_bytes, attn_stream_t stream, const void* k_new,
+               const void* v_new) {
   const int G = Hq / Hkv;
   const size_t need = attn_decode_workspace_size(B, Hq, S_max, D);
   if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
 
   attn::decode::Params p;
+  if (k_new != nullptr) {
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.kc_w = kcache;
+    p.vc_w = vcache;
+  }
   p.q = q;
   p.kc = kcache;
   p.vc = vcache;
@@ -773,6 +776,36 @@ int attn_decode(const void* q, const void* kcache, const void* vcache, const int
     return D == 64 ? launch_decode_d<__half, 64>(p, G, st) : launch_decode_d<__half, 128>(p, G, st);
   }
   return D == 64 ? launch_decode_d<float, 64>(p, G, st) : launch_decode_d<float, 128>(p, G, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_decode(const void* q, const void* kcache, const void* vcache, const int32_t* kv_lens,
+                void* o, float* lse, int B, int Hq, int Hkv, int S_max, int D, int dtype,
+                float scale, void* workspace, size_t ws_bytes, attn_stream_t stream) {
+  const int rc = decode_validate(q, kcache, vcache, kv_lens, o, lse, B, Hq, Hkv, S_max, D, dtype,
+                                 scale);
+  if (rc != ATTN_OK) return rc;
+  // the caches are only read on this path
+  return decode_run(q, const_cast<void*>(kcache), const_cast<void*>(vcache), kv_lens, o, lse, B,
+                    Hq, Hkv, S_max, D, dtype, scale, workspace, ws_bytes, stream, nullptr,
+                    nullptr);
+}
+
+int attn_decode_append(const void* q, void* kcache, void* vcache, const void* k_new,
+                       const void* v_new, const int32_t* kv_lens, void* o, float* lse, int B,
+                       int Hq, int Hkv, int S_max, int D, int dtype, float scale, void* workspace,
+                       size_t ws_bytes, attn_stream_t stream) {
+  const int rc = decode_validate(q, kcache, vcache, kv_lens, o, lse, B, Hq, Hkv, S_max, D, dtype,
+                                 scale);
+  if (rc != ATTN_OK) return rc;
+  if (!k_new || !v_new) return ATTN_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new)) return ATTN_ERR_INVALID_ARG;
+  if (dtype == ATTN_F32) return ATTN_ERR_UNSUPPORTED;
+  return decode_run(q, kcache, vcache, kv_lens, o, lse, B, Hq, Hkv, S_max, D, dtype, scale,
+                    workspace, ws_bytes, stream, k_new, v_new);
 }
 
 }  // extern "C"

@@ -59,6 +59,13 @@ struct Params {
                         // then the number of warps that took a span
   int B, Hq, Hkv, S_max, splits;  // splits = partial slots per (b, h)
   float scale_log2;     // scale * log2(e)
+  // Fused append (bf16 split only): the new token's K and V rows
+  // [B,Hkv,D], written into row kv_len - 1 of each stream, and the caches
+  // as writable pointers.  Null: the caches are only read.
+  const void* k_new = nullptr;
+  const void* v_new = nullptr;
+  void* kc_w = nullptr;
+  void* vc_w = nullptr;
 };
 
 // 32-key sub-tiles of a stream of L keys.
@@ -533,6 +540,30 @@ __global__ void __launch_bounds__(32 * MmaCfg<D, G>::kWarps)
         *reinterpret_cast<uint4*>(vt + ch * C::kTileBytes + (nkeys + rem / 8) * 128 +
                                   (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
       }
+      fence_proxy_async_shared();  // ordered before the copy that refills the stage
+      __syncwarp();
+    }
+    if (p.k_new != nullptr && cc.j == (cc.L - 1) / kSubKeys) {
+      // Fused append: the new token is the stream's last key, row L - 1.  Its
+      // K and V rows replace what the copy brought for that row (the cache's
+      // old contents) and go to the cache for later steps.  One 16-byte unit
+      // per lane: D / 8 units of K, then D / 8 of V.  Only this worker reads
+      // that row in this launch: every sub-tile belongs to one span.
+      constexpr int kUnits = D / 8;
+      const int r = (cc.L - 1) - kSubKeys * cc.j;
+      if (lane < 2 * kUnits) {
+        const bool isv = lane >= kUnits;
+        const int u = isv ? lane - kUnits : lane;
+        const size_t row = (size_t)cc.b * p.Hkv + cc.g;
+        const uint4 val =
+            reinterpret_cast<const uint4*>(isv ? p.v_new : p.k_new)[row * kUnits + u];
+        uint8_t* tile = smem + C::kOffRing + st * C::kStageBytes + (isv ? C::kKBytes : 0u) +
+                        (u >> 3) * C::kTileBytes;
+        *reinterpret_cast<uint4*>(tile + sw128(r, u & 7)) = val;
+        reinterpret_cast<uint4*>(isv ? p.vc_w : p.kc_w)[(row * p.S_max + (cc.L - 1)) * kUnits + u] =
+            val;
+      }
+      fence_proxy_async_shared();  // ordered before the copy that refills the stage
       __syncwarp();
     }
 

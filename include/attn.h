@@ -386,6 +386,44 @@ ATTN_API int attn_decode(const void* q, const void* kcache, const void* vcache,
                 void* workspace, size_t ws_bytes, attn_stream_t stream);
 
 /*
+ * attn_decode_append -- one generation step in one call: the new token's
+ * K and V rows are appended to the caches and the step's query attends over
+ * the cache including them.  "Implementing attention from scratch", KV
+ * caching (the new token's keys and values are written at the cache length,
+ * then the query attends over every cached position); "Building a causal
+ * self-attention block from scratch in PyTorch", Step 5 (KVCache.update
+ * before attention).  The same result as kv_cache_append with
+ * pos[b] = kv_lens[b] - 1 followed by attn_decode, bit for bit, with one
+ * launch less: the decode's split kernel writes the rows while it streams
+ * the cache, replacing the one row it would have read stale.
+ *
+ *   q                 [B,Hq,D]        dtype          (read)
+ *   kcache, vcache    [B,Hkv,S_max,D] dtype          (read; row kv_lens[b] - 1
+ *                                                     of each (b, KV head)
+ *                                                     written)
+ *   k_new, v_new      [B,Hkv,D]       dtype          (read: the new token)
+ *   kv_lens           [B]             int32, device  (valid rows INCLUDING the
+ *                                                     new token; clamped to
+ *                                                     [0, S_max] as in
+ *                                                     attn_decode: a sequence
+ *                                                     with kv_lens[b] <= 0
+ *                                                     appends nothing, one
+ *                                                     with kv_lens[b] > S_max
+ *                                                     writes row S_max - 1)
+ *   o, lse, scale, workspace: as for attn_decode (same workspace size)
+ *
+ * Supported: ATTN_BF16 or ATTN_F16 with the sizes and alignment of
+ * attn_decode; k_new and v_new 16-byte aligned.  ATTN_F32 returns
+ * ATTN_ERR_UNSUPPORTED (use kv_cache_append, then attn_decode).  Returns
+ * ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE or
+ * ATTN_ERR_CUDA.
+ */
+ATTN_API int attn_decode_append(const void* q, void* kcache, void* vcache, const void* k_new,
+                                const void* v_new, const int32_t* kv_lens, void* o, float* lse,
+                                int B, int Hq, int Hkv, int S_max, int D, int dtype, float scale,
+                                void* workspace, size_t ws_bytes, attn_stream_t stream);
+
+/*
  * attn_decode_noalloc -- attn_decode for callers that cannot allocate device
  * memory.  (The pages have no counterpart; this is a library convenience.)
  *

@@ -226,3 +226,19 @@ def test_fwd_host_workspace_and_rejections(lib):
     assert fh(ws=None) == 3
     assert fh(ws_bytes=need - 1) == 3
     assert fh(ws=MIS) == 3
+
+
+def test_decode_append_rejects_bad_arguments(lib):
+    need = lib.attn_decode_workspace_size(1, 2, 64, 64)
+
+    def da(kn=FAKE, vn=FAKE, D=64, dt=1, ws=FAKE, ws_bytes=need, q=FAKE):
+        return lib.attn_decode_append(q, FAKE, FAKE, kn, vn, FAKE, FAKE, None, 1, 2, 1, 64, D,
+                                      dt, 0.125, ws, ws_bytes, None)
+    assert da(q=None) == 1
+    assert da(kn=None) == 1
+    assert da(vn=MIS) == 1
+    assert da(D=96) == 2
+    assert da(dt=0) == 2                   # fp32: append, then attn_decode
+    assert da(dt=9) == 1
+    assert da(ws=None) == 3
+    assert da(ws_bytes=need - 1) == 3
