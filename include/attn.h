@@ -60,7 +60,7 @@ typedef enum {
   ATTN_OK = 0,
   ATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, ...     */
   ATTN_ERR_UNSUPPORTED = 2, /* valid request the library does not implement */
-  ATTN_ERR_WORKSPACE = 3,   /* decode workspace missing or too small        */
+  ATTN_ERR_WORKSPACE = 3,   /* workspace missing, too small or misaligned  */
   ATTN_ERR_CUDA = 4         /* CUDA runtime/driver error at or before launch */
 } attn_status;
 
