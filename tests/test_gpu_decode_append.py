@@ -71,6 +71,23 @@ def test_fused_append_equals_two_calls(E, case):
     assert torch.equal(lse.view(torch.int32), lse_ref.view(torch.int32))
 
 
+def test_fused_append_clamps_lengths_past_the_cache(E):
+    """kv_lens beyond S_max is clamped to S_max as in attn_decode: the new
+    token then lands in the cache's last row."""
+    B, Hq, Hkv, S_max, D = 3, 8, 2, 200, 128
+    q, kc, vc, kn, vn, kv = _case(torch.bfloat16, B, Hq, Hkv, S_max, D, [205, 200, 1], seed=21)
+    scale = 1.0 / math.sqrt(D)
+    kc2, vc2 = kc.clone(), vc.clone()
+    E.kv_cache_append(kc2, vc2, kn, vn, torch.clamp(kv, max=S_max) - 1)
+    o_ref, lse_ref = E.attn_decode(q, kc2, vc2, kv, scale=scale)
+    o, lse = E.attn_decode_append(q, kc, vc, kn, vn, kv, scale=scale)
+    torch.cuda.synchronize()
+    assert torch.equal(kc.view(torch.int16), kc2.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), vc2.view(torch.int16))
+    assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse_ref.view(torch.int32))
+
+
 def test_fused_append_matches_oracle(E):
     q, kc, vc, kn, vn, kv = _case(torch.bfloat16, 6, 16, 4, 900, 128,
                                   [900, 1, 0, 257, 256, 640], seed=3)
