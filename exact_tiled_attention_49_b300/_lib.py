@@ -454,8 +454,8 @@ def attn_decode(q, kcache, vcache, kv_lens, o=None, lse=None, workspace=None,
 def attn_decode_append(q, kcache, vcache, k_new, v_new, kv_lens, o=None, lse=None,
                        workspace=None, scale=None, return_lse=True, stream=None):
     """Append the new token's K/V rows (k_new, v_new [B,Hkv,D]) at row
-    kv_lens[b] - 1 of the caches and decode over kv_lens[b] rows, in one call
-    (bf16 or fp16).  kv_lens counts the new token.  Same results as
+    kv_lens[b] - 1 of the caches and decode over kv_lens[b] rows, in one
+    call.  kv_lens counts the new token.  Same results as
     kv_cache_append(pos=kv_lens - 1) followed by attn_decode.
     Returns (o [B,Hq,D], lse [B,Hq] or None)."""
     lib = load()

@@ -734,7 +734,7 @@ int decode_validate(const void* q, const void* kcache, const void* vcache,
 
 // A validated decode step (attn_decode, attn_decode_append): the workspace
 // check and the launches.  k_new / v_new non-null: the new token's rows are
-// written into the caches by the split kernel (bf16 / fp16 only).
+// used for and written into row kv_len - 1 by the split kernel.
 int decode_run(const void* q, void* kcache, void* vcache, const int32_t* kv_lens, void* o,
                float* lse, int B, int Hq, int Hkv, int S_max, int D, int dtype, float scale,
                void* workspace, size_t ws_bytes, attn_stream_t stream, const void* k_new,
@@ -803,7 +803,6 @@ int attn_decode_append(const void* q, void* kcache, void* vcache, const void* k_
   if (rc != ATTN_OK) return rc;
   if (!k_new || !v_new) return ATTN_ERR_INVALID_ARG;
   if (!aligned16(k_new) || !aligned16(v_new)) return ATTN_ERR_INVALID_ARG;
-  if (dtype == ATTN_F32) return ATTN_ERR_UNSUPPORTED;
   return decode_run(q, kcache, vcache, kv_lens, o, lse, B, Hq, Hkv, S_max, D, dtype, scale,
                     workspace, ws_bytes, stream, k_new, v_new);
 }

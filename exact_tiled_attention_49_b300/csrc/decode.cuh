@@ -59,9 +59,9 @@ struct Params {
                         // then the number of warps that took a span
   int B, Hq, Hkv, S_max, splits;  // splits = partial slots per (b, h)
   float scale_log2;     // scale * log2(e)
-  // Fused append (bf16 split only): the new token's K and V rows
-  // [B,Hkv,D], written into row kv_len - 1 of each stream, and the caches
-  // as writable pointers.  Null: the caches are only read.
+  // Fused append: the new token's K and V rows [B,Hkv,D], used for row
+  // kv_len - 1 of each stream and written there, and the caches as
+  // writable pointers.  Null: the caches are only read.
   const void* k_new = nullptr;
   const void* v_new = nullptr;
   void* kc_w = nullptr;
@@ -165,6 +165,11 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Params p) {
   const T* vbase = reinterpret_cast<const T*>(p.vc) + kv_row0 * D;
   const int w_begin = k_begin + warp * 32;
   const int nk = max(0, min(32, k_end - w_begin));
+  // Fused append: row L - 1 is the new token; it is taken from k_new / v_new
+  // (this warp alone reads that row in this launch) and written to the
+  // caches below.
+  const int jn = p.k_new != nullptr ? L - 1 : -1;
+  const size_t new_row = ((size_t)b * p.Hkv + g) * D;
 
   // Scores: lane -> key.
   float s[G];
@@ -172,7 +177,8 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Params p) {
   for (int h = 0; h < G; ++h) s[h] = 0.f;
   const int j = w_begin + lane;
   if (lane < nk) {
-    const uint4* kr = reinterpret_cast<const uint4*>(kbase + (size_t)j * D);
+    const uint4* kr = reinterpret_cast<const uint4*>(
+        j == jn ? reinterpret_cast<const T*>(p.k_new) + new_row : kbase + (size_t)j * D);
 #pragma unroll 4
     for (int c = 0; c < NV; ++c) {
       float kf[VEC];
@@ -211,7 +217,9 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Params p) {
 #pragma unroll 4
   for (int jj = 0; jj < nk; ++jj) {
     float vf[DPL];
-    load_lane<T, DPL>(vbase + (size_t)(w_begin + jj) * D, lane, vf);
+    load_lane<T, DPL>(w_begin + jj == jn ? reinterpret_cast<const T*>(p.v_new) + new_row
+                                         : vbase + (size_t)(w_begin + jj) * D,
+                      lane, vf);
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       const float pb = __shfl_sync(0xffffffffu, pw[h], jj);
@@ -223,6 +231,15 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(Params p) {
   for (int h = 0; h < G; ++h)
 #pragma unroll
     for (int e = 0; e < DPL; ++e) red_o[(warp * G + h) * D + lane * DPL + e] = acc[h][e];
+  if (jn >= w_begin && jn < w_begin + nk) {
+    const size_t dst = (kv_row0 + jn) * NV;
+    for (int c = lane; c < NV; c += 32) {
+      reinterpret_cast<uint4*>(p.kc_w)[dst + c] =
+          reinterpret_cast<const uint4*>(p.k_new)[new_row / VEC + c];
+      reinterpret_cast<uint4*>(p.vc_w)[dst + c] =
+          reinterpret_cast<const uint4*>(p.v_new)[new_row / VEC + c];
+    }
+  }
   __syncthreads();
 
   // Merge the warps of this chunk into one partial per head.

@@ -412,11 +412,9 @@ ATTN_API int attn_decode(const void* q, const void* kcache, const void* vcache,
  *                                                     writes row S_max - 1)
  *   o, lse, scale, workspace: as for attn_decode (same workspace size)
  *
- * Supported: ATTN_BF16 or ATTN_F16 with the sizes and alignment of
- * attn_decode; k_new and v_new 16-byte aligned.  ATTN_F32 returns
- * ATTN_ERR_UNSUPPORTED (use kv_cache_append, then attn_decode).  Returns
- * ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE or
- * ATTN_ERR_CUDA.
+ * Supported: the types, sizes and alignment of attn_decode; k_new and
+ * v_new 16-byte aligned.  Returns ATTN_OK, ATTN_ERR_INVALID_ARG,
+ * ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE or ATTN_ERR_CUDA.
  */
 ATTN_API int attn_decode_append(const void* q, void* kcache, void* vcache, const void* k_new,
                                 const void* v_new, const int32_t* kv_lens, void* o, float* lse,

@@ -238,7 +238,6 @@ def test_decode_append_rejects_bad_arguments(lib):
     assert da(kn=None) == 1
     assert da(vn=MIS) == 1
     assert da(D=96) == 2
-    assert da(dt=0) == 2                   # fp32: append, then attn_decode
     assert da(dt=9) == 1
     assert da(ws=None) == 3
     assert da(ws_bytes=need - 1) == 3

@@ -35,6 +35,8 @@ CASES = [
     (torch.bfloat16, 5, 32, 8, 700, 128, [1, 32, 33, 700, 0]),       # sub-tile edges, empty
     (torch.bfloat16, 3, 8, 8, 300, 64, [299, 64, 17]),
     (torch.float16, 4, 16, 1, 1000, 128, [1000, 513, 2, 999]),       # G = 16
+    (torch.float32, 3, 8, 2, 600, 64, [600, 257, 256]),              # the fp32 split kernel
+    (torch.float32, 2, 4, 4, 300, 128, [1, 0]),
     (torch.bfloat16, 64, 32, 8, 8193, 128, None),                   # the GQA decode workload's shape
 ]
 
@@ -65,9 +67,10 @@ def test_fused_append_equals_two_calls(E, case):
     o, lse = E.attn_decode_append(q, kc, vc, kn, vn, kv, scale=scale)
     torch.cuda.synchronize()
     assert E.attn_kernel_launches() - before == 2          # split + merge, no append launch
-    assert torch.equal(kc.view(torch.int16), kc2.view(torch.int16))
-    assert torch.equal(vc.view(torch.int16), vc2.view(torch.int16))
-    assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+    iv = torch.int32 if dtype == torch.float32 else torch.int16
+    assert torch.equal(kc.view(iv), kc2.view(iv))
+    assert torch.equal(vc.view(iv), vc2.view(iv))
+    assert torch.equal(o.view(iv), o_ref.view(iv))
     assert torch.equal(lse.view(torch.int32), lse_ref.view(torch.int32))
 
 
