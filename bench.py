@@ -623,6 +623,7 @@ def other_workloads(E, skip, device, steps, peaks):
     out.update(backward_workloads(E, device, steps, peaks, flush))
     out.update(fp8_workloads(E, device, steps, peaks, flush))
     out.update(chunked_workloads(E, device, steps, peaks, flush))
+    out.update(shard_workloads(E, device, steps, peaks, flush))
     if E.attn_device_error(clear=True) != 0:
         raise RuntimeError("device error while timing the other workloads")
     return out
@@ -738,6 +739,65 @@ def chunked_workloads(E, device, steps, peaks, flush):
                          "kernel": "fwd_bf16_tc_kernel<128,0,0> (q_pos)",
                          "frac": v_ / peaks["bf16_tflops"]}}
     del q, k, v, o, lse, graph
+    torch.cuda.empty_cache()
+    return out
+
+
+def shard_workloads(E, device, steps, peaks, flush):
+    """The single-GPU half of sequence parallelism: the long-context prefill
+    (B=1 H=16 T=S=32768 D=128, Q x 2) computed as 4 key shards of 8192 keys
+    (attn_fwd_kv_shard at global offsets 0, 8192, 16384, 24576, each
+    partial normalised over its shard) and their LSE merge (attn_lse_merge).
+    One CUDA graph of the five calls per step, L2 flushed; throughput counts
+    the prefill's own FLOPs, so the merge and the shards' tails show as
+    the difference from the unsharded prefill."""
+    import torch
+    import workloads
+    w = workloads.WORKLOADS[3]
+    x = workloads.workload_inputs(3, device=device)
+    n = 4
+    S1 = w.S // n
+    q = x["q"]
+    ks = [x["k"][:, :, i * S1:(i + 1) * S1].contiguous() for i in range(n)]
+    vs = [x["v"][:, :, i * S1:(i + 1) * S1].contiguous() for i in range(n)]
+    del x
+    q_pos = torch.zeros((w.B,), dtype=torch.int32, device=device)
+    key_lens = torch.full((w.B,), w.S, dtype=torch.int32, device=device)
+    o_parts = torch.empty((n,) + tuple(q.shape), dtype=q.dtype, device=device)
+    lse_parts = torch.empty((n,) + tuple(q.shape[:3]), dtype=torch.float32, device=device)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=device)
+    scale = 1.0 / math.sqrt(w.D)
+
+    def step():
+        for i in range(n):
+            E.attn_fwd_kv_shard(q, ks[i], vs[i], q_pos, key_lens, i * S1, o=o_parts[i],
+                                lse=lse_parts[i], causal=True, scale=scale)
+        E.attn_lse_merge(o_parts, lse_parts, o=o, lse=lse)
+    for _ in range(3):
+        step()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    total = 0.0
+    for _ in range(steps):
+        flush.zero_()
+        e0.record()
+        graph.replay()
+        e1.record()
+        e1.synchronize()
+        total += e0.elapsed_time(e1)
+    ms = total / steps
+    v_ = prefill_flops(w, None) / (ms * 1e-3) / 1e12
+    out = {"shard4_3": {"workload": f"{w.name} as {n} key shards of {S1} keys + LSE merge",
+                        "value": v_, "unit": "TFLOPS", "ms": ms,
+                        "kernel": "fwd_bf16_tc_kernel<128,0,0> (key shards) + lse_merge_kernel",
+                        "frac": v_ / peaks["bf16_tflops"]}}
+    del q, ks, vs, o_parts, lse_parts, o, lse, graph
     torch.cuda.empty_cache()
     return out
 
