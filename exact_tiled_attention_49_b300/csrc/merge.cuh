@@ -8,9 +8,12 @@
 // Stable softmax; "Building a causal self-attention block from scratch in
 // PyTorch", Extending It: sharding Q/K/V across devices and recombining):
 //     LSE = ln sum_n exp(LSE_n),   O = sum_n exp(LSE_n - LSE) O_n.
-// The partials are visited in order with a running maximum, so no exponent
-// overflows; a partial with LSE_n = -inf (its rows saw no key) adds nothing,
-// and a row that no partial saw is O = 0, LSE = -inf.
+// Two passes over a row's partials: their maximum M, then the sum in order
+// n = 0, 1, ... with weights exp(LSE_n - M) <= 1, so no exponent overflows;
+// a partial with LSE_n = -inf (its rows saw no key) adds nothing, and a row
+// that no partial saw is O = 0, LSE = -inf.  The loads of one pass do not
+// depend on each other, so a thread has all of a row's partials in flight
+// at once (the merge is bound by memory, not arithmetic).
 #pragma once
 
 #include "common.cuh"
@@ -74,22 +77,23 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(Params p) {
 #pragma unroll
     for (int e = 0; e < V; ++e) acc[e] = 0.f;
     float m = -INFINITY, l = 0.f;
-    for (int n = 0; n < p.n_parts; ++n) {
-      const float x = p.lse_parts[(long long)n * p.rows + row];
-      if (!(x > -INFINITY)) continue;  // no key in this partial (or NaN): nothing to add
-      if (x > m) {
-        const float r = expf(m - x);   // 0 while nothing was added yet
+#pragma unroll 4
+    for (int n = 0; n < p.n_parts; ++n)  // NaN (never written) is ignored by fmaxf
+      m = fmaxf(m, p.lse_parts[(long long)n * p.rows + row]);
+    if (m > -INFINITY) {
+#pragma unroll 4
+      for (int n = 0; n < p.n_parts; ++n) {
+        const float x = p.lse_parts[(long long)n * p.rows + row];
+        // no key in this partial (or NaN): weight 0, and its O is not read
+        const float w = (x > -INFINITY) ? expf(x - m) : 0.f;
+        if (w > 0.f) {
+          float f[V];
+          E::unpack(parts[((long long)n * p.rows + row) * per_row + c], f);
 #pragma unroll
-        for (int e = 0; e < V; ++e) acc[e] *= r;
-        l *= r;
-        m = x;
+          for (int e = 0; e < V; ++e) acc[e] = fmaf(w, f[e], acc[e]);
+          l += w;
+        }
       }
-      const float w = expf(x - m);
-      float f[V];
-      E::unpack(parts[((long long)n * p.rows + row) * per_row + c], f);
-#pragma unroll
-      for (int e = 0; e < V; ++e) acc[e] = fmaf(w, f[e], acc[e]);
-      l += w;
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll

@@ -268,8 +268,9 @@ ATTN_API int attn_fwd_kv_shard(const void* q, const void* k, const void* v, void
  * exp(m_old - m_new)):
  *     LSE = ln sum_n exp(LSE_n),   O = sum_n exp(LSE_n - LSE) O_n
  * Partials with LSE_n = -inf add nothing; a row with no partial is written as
- * O = 0, LSE = -inf.  Partials are visited in order n = 0 .. n_parts - 1
- * with a running maximum (float32 arithmetic, output rounded once).
+ * O = 0, LSE = -inf.  Per row: the maximum M of the partials' LSE, then
+ * the sum over n = 0 .. n_parts - 1 in order with weights exp(LSE_n - M)
+ * (float32 arithmetic, output rounded once).
  *
  *   o_parts    [n_parts,B,Hq,T,D]  dtype    (read)
  *   lse_parts  [n_parts,B,Hq,T]    float32  (read)
