@@ -276,7 +276,8 @@ int launch_bwd_tc(const attn::tcbwd::Params& p0, const void* q, const void* k, c
       !make_tmap_bf16(&tv, v, D, p0.S, (long long)p0.B * p0.Hkv, kF16))
     return ATTN_ERR_CUDA;
   const long long rows = (long long)p0.B * p0.Hq * p0.T;
-  const long long want_blocks = (rows + 7) / 8;  // 8 warps per block, one row per warp
+  const long long rows_per_block = 8 * (32 / (D / 8));  // 8 warps, 32 / (D / 8) rows each
+  const long long want_blocks = (rows + rows_per_block - 1) / rows_per_block;
   const unsigned blocks = (unsigned)std::min<long long>(want_blocks, (long long)num_sms() * 16);
   bwd_delta_kernel<kF16><<<blocks, 256, 0, st>>>(p0, rows);
   int rc = launch_status();

@@ -67,19 +67,24 @@ __device__ __forceinline__ int q_offset(const Params& p, int b) {
 }
 
 // ------------------------------------------------------------ delta pass
-// One warp per row: delta[row] = sum_d dO[row,d] * O[row,d] in fp32.
+// delta[row] = sum_d dO[row,d] * O[row,d] in fp32.  A row is D / 8 lanes of
+// one 16-byte vector each (16 lanes at D = 128, 8 at D = 64), so a warp
+// takes 32 / (D / 8) rows at a time with every lane loading; the lanes of a
+// row add their partial dot products with xor shuffles inside their group.
 template <bool kF16>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(Params p, long long rows) {
+  const int lpr = p.D / 8;   // lanes per row
+  const int rpw = 32 / lpr;  // rows per warp step
   const long long warp_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
   const long long n_warps = ((long long)gridDim.x * blockDim.x) >> 5;
-  for (long long r = warp_id; r < rows; r += n_warps) {
-    const uint16_t* orow = reinterpret_cast<const uint16_t*>(p.o) + r * p.D;
-    const uint16_t* drow = reinterpret_cast<const uint16_t*>(p.dout) + r * p.D;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane / lpr, c = lane - sub * lpr;
+  for (long long r0 = warp_id * rpw; r0 < rows; r0 += n_warps * rpw) {
+    const long long r = r0 + sub;
     float acc = 0.f;
-    for (int d = lane * 8; d < p.D; d += 256) {
-      const uint4 a = *reinterpret_cast<const uint4*>(orow + d);
-      const uint4 g = *reinterpret_cast<const uint4*>(drow + d);
+    if (r < rows) {
+      const uint4 a = reinterpret_cast<const uint4*>(p.o)[r * lpr + c];
+      const uint4 g = reinterpret_cast<const uint4*>(p.dout)[r * lpr + c];
       acc = fmaf(elem_lo<kF16>(a.x), elem_lo<kF16>(g.x), acc);
       acc = fmaf(elem_hi<kF16>(a.x), elem_hi<kF16>(g.x), acc);
       acc = fmaf(elem_lo<kF16>(a.y), elem_lo<kF16>(g.y), acc);
@@ -89,8 +94,8 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(Params p, long long rows
       acc = fmaf(elem_lo<kF16>(a.w), elem_lo<kF16>(g.w), acc);
       acc = fmaf(elem_hi<kF16>(a.w), elem_hi<kF16>(g.w), acc);
     }
-    acc = warp_sum(acc);
-    if (lane == 0) p.delta[r] = acc;
+    for (int off = lpr >> 1; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (c == 0 && r < rows) p.delta[r] = acc;
   }
 }
 
