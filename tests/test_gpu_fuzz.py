@@ -1,5 +1,6 @@
-"""Seeded random shapes through every forward entry point, compared with the
-float64 oracle under the parity tolerances of tests/parity.py.
+"""Seeded random shapes through every forward entry point and the backward,
+compared with the float64 oracle under the parity tolerances of
+tests/parity.py (the backward: those of tests/test_gpu_bwd.py).
 
 The fixed cases elsewhere pin the paths the kernels take (tile boundaries,
 padding, item walks at full size); these draws add shapes no one picked:
@@ -114,3 +115,47 @@ def test_fuzz_host(E, seed):
     torch.cuda.current_stream().synchronize()
     o_ref, lse_ref = oracle_fwd(q, k, v, causal, torch.from_numpy(lens), scale)
     compare(o, lse, o_ref, lse_ref, dtype, what=f"host seed {seed}")
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_fuzz_backward(E, seed):
+    """attn_bwd on seeded random shapes (bf16), with the bound of
+    tests/test_gpu_bwd.py: 2 u A elementwise, 1e-2 normwise."""
+    import oracle
+    from test_gpu_bwd import check_grad
+    from workloads import to_numpy_exact
+    rng = np.random.default_rng(5000 + seed)
+    D = int(rng.choice([64, 128]))
+    Hkv = int(rng.integers(1, 3))
+    Hq = Hkv * int(rng.choice([1, 2, 4]))
+    B = int(rng.integers(1, 3))
+    T = int(rng.integers(1, 321))
+    S = int(rng.integers(1, 361))
+    causal = bool(rng.integers(0, 2))
+    kl = torch.from_numpy(rng.integers(0, S + 1, size=B).astype(np.int32)).cuda()
+    qp = None
+    if rng.integers(0, 2):
+        qp = torch.from_numpy(np.array([int(rng.integers(-T, S + 1)) for _ in range(B)],
+                                       dtype=np.int32)).cuda()
+    q, k, v = _tensors(B, Hq, Hkv, T, S, D, torch.bfloat16, seed)
+    g = torch.Generator(device="cuda").manual_seed(7000 + seed)
+    dout = torch.randn(B, Hq, T, D, generator=g, device="cuda").to(torch.bfloat16)
+    scale = 1.0 / math.sqrt(D)
+    if qp is None:
+        o, lse = E.attn_fwd(q, k, v, causal=causal, key_lens=kl, scale=scale)
+    else:
+        o, lse = E.attn_fwd_chunked(q, k, v, qp, kl, causal=causal, scale=scale)
+    dq, dk, dv = E.attn_bwd(q, k, v, o, dout, lse, causal=causal, key_lens=kl, q_pos=qp,
+                            scale=scale)
+    torch.cuda.synchronize()
+    assert E.attn_device_error(clear=True) == 0
+    bits = [to_numpy_exact(t)[0] for t in (q, k, v, dout)]
+    kw = dict(causal=causal, key_lens=kl.cpu().numpy(), scale=scale, bf16=True,
+              q_pos=None if qp is None else qp.cpu().numpy())
+    rq, rk, rv, _, rl = oracle.attn_bwd_np(*bits, **kw)
+    aq, ak, av = oracle.attn_bwd_magnitudes_np(*bits, **kw)
+    check_grad(dq, rq, aq, f"dq seed {seed}")
+    check_grad(dk, rk, ak, f"dk seed {seed}")
+    check_grad(dv, rv, av, f"dv seed {seed}")
+    empty = ~np.isfinite(rl)
+    assert np.all(dq.double().cpu().numpy()[empty] == 0)
