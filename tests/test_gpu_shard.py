@@ -138,3 +138,31 @@ def test_shard_rejects_bad_arguments(E):
         E.attn_fwd_kv_shard(y, y, y, qp, qp, 0)      # D = 96 unsupported
     assert ex.value.status == E.ATTN_ERR_UNSUPPORTED
     assert TOL  # the shared tolerances are the ones used above
+
+
+@pytest.mark.timeout(600)
+def test_ring_attention_default_kernels_one_rank(E, tmp_path):
+    """ring.ring_attention with its default per-shard compute and merge (this
+    library's kernels) in a one-rank NCCL group: one shard holding every key,
+    merged alone, equals the oracle's attention.  (Several ranks need several
+    GPUs; the exchange order is tested on the CPU with gloo.)"""
+    import torch.distributed as dist
+    from exact_tiled_attention_49_b300.ring import ring_attention
+    store = dist.FileStore(str(tmp_path / "store"), 1)
+    dist.init_process_group("nccl", store=store, rank=0, world_size=1,
+                            device_id=torch.device("cuda", 0))
+    try:
+        B, Hq, Hkv, T, S, D = 2, 4, 2, 200, 500, 128
+        g = torch.Generator(device="cuda").manual_seed(77)
+        q = _rand(B, Hq, T, D, "bf16", g)
+        k = _rand(B, Hkv, S, D, "bf16", g)
+        v = _rand(B, Hkv, S, D, "bf16", g)
+        lens = torch.tensor([500, 333], dtype=torch.int32, device="cuda")
+        q_pos = lens - T   # bottom-right: each sequence's queries end at its last key
+        scale = 1.0 / math.sqrt(D)
+        o, lse = ring_attention(q, k, v, q_pos, lens, [0], causal=True, scale=scale)
+        torch.cuda.synchronize()
+        o_ref, lse_ref = oracle_fwd(q, k, v, True, lens, scale, q_pos=q_pos)
+        compare(o, lse, o_ref, lse_ref, torch.bfloat16, what="ring_attention, one rank")
+    finally:
+        dist.destroy_process_group()
