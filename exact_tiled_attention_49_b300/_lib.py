@@ -374,7 +374,8 @@ def attn_bwd_workspace_size(B: int, Hq: int, T: int) -> int:
 def attn_bwd(q, k, v, o, dout, lse, causal=False, key_lens=None, q_pos=None, scale=None,
              dq=None, dk=None, dv=None, workspace=None, stream=None):
     """Backward pass: (dq, dk, dv) for attn_fwd's (o, lse) and the gradient
-    dout of its output.  q/o/dout [B,Hq,T,D], k/v [B,Hkv,S,D] (bf16, CUDA);
+    dout of its output.  q/o/dout [B,Hq,T,D], k/v [B,Hkv,S,D] (bf16, fp16 or
+    fp32, CUDA);
     key_lens / q_pos as for attn_fwd / attn_fwd_chunked."""
     lib = load()
     B, Hq, T, D = q.shape

@@ -19,6 +19,7 @@
 #include "../../include/attn.h"
 #include "append.cuh"
 #include "bwd_bf16_tc.cuh"
+#include "bwd_f32.cuh"
 #include "common.cuh"
 #include "decode.cuh"
 #include "fwd_bf16_tc.cuh"
@@ -290,6 +291,69 @@ int launch_bwd_tc(const attn::tcbwd::Params& p0, const void* q, const void* k, c
   kdkdv<<<dim3(p0.B * p0.Hkv, p0.n_ktiles), kThreads, Cfg<D>::kSmemAlloc, st>>>(tq, tdo, tk, tv,
                                                                                p0);
   return launch_status();
+}
+
+// Exact fp32 backward (bwd_f32.cuh): any 1 <= D <= 256, 4-byte alignment.
+template <int NC>
+int launch_bwd_f32(const attn::f32bwd::Params& p, cudaStream_t st) {
+  using namespace attn::f32bwd;
+  const size_t smem = (size_t)kWarps * 2 * p.D * sizeof(float);
+  bwd_f32_dq_kernel<NC><<<dim3((p.T + kWarps - 1) / kWarps, p.Hq, p.B), kThreads, smem, st>>>(p);
+  int rc = launch_status();
+  if (rc != ATTN_OK) return rc;
+  bwd_f32_dkdv_kernel<NC><<<dim3((p.S + kWarps - 1) / kWarps, p.Hkv, p.B), kThreads, smem, st>>>(p);
+  return launch_status();
+}
+
+int bwd_f32(const void* q, const void* k, const void* v, const void* o, const void* dout,
+            const float* lse, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int T, int S,
+            int D, int causal, const int32_t* key_lens, const int32_t* q_pos, float scale,
+            void* workspace, size_t ws_bytes, attn_stream_t stream) {
+  if (D > 256) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned4(q) || !aligned4(k) || !aligned4(v) || !aligned4(o) || !aligned4(dout) ||
+      !aligned4(dq) || !aligned4(dk) || !aligned4(dv) || !aligned4(lse) ||
+      (key_lens != nullptr && !aligned4(key_lens)) || (q_pos != nullptr && !aligned4(q_pos)))
+    return ATTN_ERR_INVALID_ARG;
+  const size_t need = ((size_t)B * Hq * T * sizeof(float) + 15) / 16 * 16;
+  if (workspace == nullptr || ws_bytes < need || !aligned16(workspace)) return ATTN_ERR_WORKSPACE;
+  attn::f32bwd::Params p{};
+  p.q = static_cast<const float*>(q);
+  p.k = static_cast<const float*>(k);
+  p.v = static_cast<const float*>(v);
+  p.o = static_cast<const float*>(o);
+  p.dout = static_cast<const float*>(dout);
+  p.lse = lse;
+  p.delta = static_cast<float*>(workspace);
+  p.dq = static_cast<float*>(dq);
+  p.dk = static_cast<float*>(dk);
+  p.dv = static_cast<float*>(dv);
+  p.key_lens = key_lens;
+  p.q_pos = q_pos;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.T = T;
+  p.S = S;
+  p.D = D;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const long long rows = (long long)B * Hq * T;
+  attn::f32bwd::bwd_f32_delta_kernel<<<(unsigned)((rows + attn::f32bwd::kWarps - 1) /
+                                                  attn::f32bwd::kWarps),
+                                       attn::f32bwd::kThreads, 0, st>>>(p, rows);
+  const int rc = launch_status();
+  if (rc != ATTN_OK) return rc;
+  switch ((D + 31) / 32) {
+    case 1: return launch_bwd_f32<1>(p, st);
+    case 2: return launch_bwd_f32<2>(p, st);
+    case 3: return launch_bwd_f32<3>(p, st);
+    case 4: return launch_bwd_f32<4>(p, st);
+    case 5: return launch_bwd_f32<5>(p, st);
+    case 6: return launch_bwd_f32<6>(p, st);
+    case 7: return launch_bwd_f32<7>(p, st);
+    default: return launch_bwd_f32<8>(p, st);
+  }
 }
 
 // -------------------------------------------------------------- decode
@@ -662,8 +726,11 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const v
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || S <= 0 || D <= 0) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0 || !finite_positive(scale)) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_F16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
-  if (dtype == ATTN_F32 || (D != 64 && D != 128)) return ATTN_ERR_UNSUPPORTED;
   if (B > 65535 || Hq > 65535 || Hkv > 65535) return ATTN_ERR_UNSUPPORTED;
+  if (dtype == ATTN_F32)
+    return bwd_f32(q, k, v, o, dout, lse, dq, dk, dv, B, Hq, Hkv, T, S, D, causal, key_lens,
+                   q_pos, scale, workspace, ws_bytes, stream);
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
   if ((long long)B * Hq > 0x7fffffffll || (T + 127) / 128 > 65535 || (S + 127) / 128 > 65535)
     return ATTN_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) ||

@@ -324,12 +324,16 @@ ATTN_API size_t attn_bwd_workspace_size(int B, int Hq, int T);
  *                            (q_pos NULL = bottom-right, S - T)
  *   workspace   >= attn_bwd_workspace_size(B, Hq, T) bytes, 16-byte aligned
  *
- * Supported: ATTN_BF16 or ATTN_F16 with D in {64, 128} (tcgen05 tensor
- * cores, fp32 accumulation; P and dS are rounded to the input type for the
- * products); all
- * pointers 16-byte aligned (lse, key_lens, q_pos: 4); B * Hq < 2^31 and at
- * most 65535 tiles of 128 rows in T and in S.  ATTN_F32 returns
- * ATTN_ERR_UNSUPPORTED.  No atomics: results do not depend on scheduling.
+ * Supported:
+ *   ATTN_BF16, ATTN_F16: D in {64, 128} (tcgen05 tensor cores, fp32
+ *              accumulation; P and dS are rounded to the input type for the
+ *              products); all pointers 16-byte aligned (lse, key_lens,
+ *              q_pos: 4); B * Hq < 2^31 and at most 65535 tiles of 128 rows
+ *              in T and in S.
+ *   ATTN_F32:  1 <= D <= 256, 4-byte aligned; exact float32 on the CUDA
+ *              cores (FFMA, accurate expf, no TF32), the counterpart of the
+ *              fp32 forward.
+ * No atomics: results do not depend on scheduling.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED,
  * ATTN_ERR_WORKSPACE or ATTN_ERR_CUDA.
  */

@@ -176,8 +176,10 @@ def test_bwd_rejects_bad_arguments(lib):
                             dt, 1, None, None, 0.125, ws, ws_bytes, None)
     assert bw(dq=None) == 1
     assert bw(Hq=3, Hkv=2) == 1
-    assert bw(dt=0) == 2                   # fp32 backward is not built
-    assert bw(D=96) == 2
+    assert bw(dt=0, D=300) == 2            # fp32: D <= 256
+    assert bw(dt=0, dq=MIS) == 1           # fp32: 4-byte alignment
+    assert bw(dt=0, ws=None) == 3
+    assert bw(D=96) == 2                   # bf16 / fp16: D in {64, 128}
     assert bw(ws=None) == 3
     assert bw(ws_bytes=need - 4) == 3
 

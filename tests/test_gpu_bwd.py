@@ -117,11 +117,70 @@ def test_backward(E, case):
 def test_backward_rejects_bad_arguments(E):
     x = torch.zeros(1, 1, 128, 64, dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros(1, 1, 128, device="cuda")
-    with pytest.raises(E.AttnError):   # fp32 is not supported by the backward
-        xf = x.float()
+    with pytest.raises(E.AttnError):   # fp32 takes D <= 256
+        xf = torch.zeros(1, 1, 128, 260, device="cuda")
         E.attn_bwd(xf, xf, xf, xf, xf, lse)
     with pytest.raises(E.AttnError):   # D must be 64 or 128
         y = torch.zeros(1, 1, 128, 32, dtype=torch.bfloat16, device="cuda")
         E.attn_bwd(y, y, y, y, y, lse)
     with pytest.raises(E.AttnError):   # workspace too small
         E.attn_bwd(x, x, x, x, x, lse, workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+
+
+F32_CASES = [
+    # (B, Hq, Hkv, T, S, D, causal, key_lens, q_pos)
+    (2, 4, 2, 130, 200, 64, True, [200, 77], None),
+    (1, 2, 1, 100, 300, 37, False, [250], None),
+    (2, 2, 2, 150, 150, 128, True, None, [10, -20]),
+    (1, 8, 2, 90, 90, 256, True, None, None),
+    (2, 3, 3, 33, 65, 1, True, [65, 0], None),
+]
+
+
+@pytest.mark.parametrize("case", F32_CASES, ids=lambda c: "x".join(map(str, c[:6])))
+def test_backward_fp32(E, case):
+    """The exact fp32 backward (CUDA cores).  Bound, derived: with fp32's unit
+    roundoff u = 2^-24, dot products of D terms and sums over at most n rows
+    or keys with fused multiply-adds, the forward's fp32 O and LSE, and
+    accurate expf (a few ulp), every element is within 4 (D + n) u A of the
+    float64 result, A the sum of absolute terms (oracle.attn_bwd_magnitudes_np);
+    normwise 1e-5."""
+    B, Hq, Hkv, T, S, D, causal, lens, qpos = case
+    g = torch.Generator(device="cuda").manual_seed(43)
+    q = torch.randn(B, Hq, T, D, generator=g, device="cuda")
+    k = torch.randn(B, Hkv, S, D, generator=g, device="cuda")
+    v = torch.randn(B, Hkv, S, D, generator=g, device="cuda")
+    dout = torch.randn(B, Hq, T, D, generator=g, device="cuda")
+    kl = None if lens is None else torch.tensor(lens, dtype=torch.int32, device="cuda")
+    qp = None if qpos is None else torch.tensor(qpos, dtype=torch.int32, device="cuda")
+    if kl is not None:
+        for b in range(B):   # rows past the valid length may hold anything
+            k[b, :, int(kl[b]):] = float("nan")
+            v[b, :, int(kl[b]):] = float("nan")
+    scale = 1.0 / math.sqrt(D)
+    if qp is None:
+        o, lse = E.attn_fwd(q, k, v, causal=causal, key_lens=kl, scale=scale)
+    else:
+        klc = kl if kl is not None else torch.full((B,), S, dtype=torch.int32, device="cuda")
+        o, lse = E.attn_fwd_chunked(q, k, v, qp, klc, causal=causal, scale=scale)
+    dq, dk, dv = E.attn_bwd(q, k, v, o, dout, lse, causal=causal, key_lens=kl, q_pos=qp,
+                            scale=scale)
+    torch.cuda.synchronize()
+    assert E.attn_device_error(clear=True) == 0
+    arr = [t.cpu().numpy() for t in (q, k, v, dout)]
+    kw = dict(causal=causal, key_lens=None if kl is None else kl.cpu().numpy(), scale=scale,
+              bf16=False, q_pos=None if qp is None else qp.cpu().numpy())
+    rq, rk, rv, _, rl = oracle.attn_bwd_np(*arr, **kw)
+    aq, ak, av = oracle.attn_bwd_magnitudes_np(*arr, **kw)
+    n = max(S, T * (Hq // Hkv))
+    for gg, ref, mag, name in ((dq, rq, aq, "dq"), (dk, rk, ak, "dk"), (dv, rv, av, "dv")):
+        x = gg.double().cpu().numpy()
+        assert np.isfinite(x).all(), name
+        err = np.abs(x - ref)
+        assert (err <= 4 * (D + n) * 2.0 ** -24 * mag + 1e-30).all(), \
+            f"{name}: max err {err.max():.3g}"
+        nref = np.linalg.norm(ref)
+        if nref > 0:
+            assert np.linalg.norm(x - ref) / nref <= 1e-5, name
+    empty = ~np.isfinite(rl)
+    assert np.all(dq.double().cpu().numpy()[empty] == 0)
