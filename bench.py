@@ -624,6 +624,7 @@ def other_workloads(E, skip, device, steps, peaks):
     out.update(fp8_workloads(E, device, steps, peaks, flush))
     out.update(chunked_workloads(E, device, steps, peaks, flush))
     out.update(shard_workloads(E, device, steps, peaks, flush))
+    out.update(long_decode_workloads(E, device, steps, peaks))
     if E.attn_device_error(clear=True) != 0:
         raise RuntimeError("device error while timing the other workloads")
     return out
@@ -798,6 +799,51 @@ def shard_workloads(E, device, steps, peaks, flush):
                         "kernel": "fwd_bf16_tc_kernel<128,0,0> (key shards) + lse_merge_kernel",
                         "frac": v_ / peaks["bf16_tflops"]}}
     del q, ks, vs, o_parts, lse_parts, o, lse, graph
+    torch.cuda.empty_cache()
+    return out
+
+
+def long_decode_workloads(E, device, steps, peaks):
+    """One long sequence: the GQA decode step (Hq=32 Hkv=8 D=128 bf16) of a
+    single sequence with 131071 cached tokens plus the new one, where the
+    balanced spans split one sequence's 8 streams over every SM.  Steps
+    (attn_decode_append) back to back in one CUDA graph (the 537 MB cache is
+    four times L2)."""
+    import torch
+    import workloads
+    d = workloads.decode_inputs(1, 32, 8, 128, 131071, 131071, "bf16", seed=9, device=device)
+    ws = torch.empty(E.attn_decode_workspace_size(1, 32, d["S_max"], 128), dtype=torch.uint8,
+                     device=device)
+    o = torch.empty_like(d["q"])
+    lse = torch.empty((1, 32), dtype=torch.float32, device=device)
+    scale = 1.0 / math.sqrt(128)
+
+    def step():
+        E.attn_decode_append(d["q"], d["kcache"], d["vcache"], d["k_new"], d["v_new"], d["kv_len"],
+                             o=o, lse=lse, workspace=ws, scale=scale)
+    for _ in range(3):
+        step()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(steps):
+            step()
+    graph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    graph.replay()
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = float(d["kv_len"].sum().item()) * 8 * 128 * 2 * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out = {"decode_long": {"workload": "GQA decode, one sequence of 131072 tokens, Hq=32 Hkv=8 "
+                                       "D=128 bf16 (attn_decode_append)",
+                           "value": gbs, "unit": "GB/s", "ms": ms,
+                           "kernel": "decode_split_mma_kernel<128,4,0>+decode_combine_spans_kernel",
+                           "frac": gbs / peaks["hbm_gbs"]}}
+    del d, ws, o, lse, graph
     torch.cuda.empty_cache()
     return out
 

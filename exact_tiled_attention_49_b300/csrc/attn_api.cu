@@ -381,9 +381,13 @@ int launch_decode_g(const attn::decode::Params& p, cudaStream_t st) {
     const long long ctas = std::max<long long>(1, std::min<long long>(num_sms(), want));
     launch_pdl(kernel, dim3((unsigned)ctas), dim3(32 * C::kWarps), C::kSmemBytes, st, tk, tv, p);
     if (launch_status() != ATTN_OK) return ATTN_ERR_CUDA;
-    const long long heads = (long long)p.B * p.Hq;  // one warp each
-    launch_pdl(decode_combine_spans_kernel<T, D>, dim3((unsigned)((heads + 7) / 8)), dim3(256), 0,
-               st, p);
+    const long long heads = (long long)p.B * p.Hq;
+    if ((long long)p.B * p.Hkv * 8 < ctas * C::kWarps)
+      // few, long streams (more than ~8 pieces each): a block per head
+      launch_pdl(decode_combine_heads_kernel<T, D>, dim3((unsigned)heads), dim3(256), 0, st, p);
+    else  // one warp per head
+      launch_pdl(decode_combine_spans_kernel<T, D>, dim3((unsigned)((heads + 7) / 8)), dim3(256),
+                 0, st, p);
     return launch_status();
   } else {
     // fp32: one block per (chunk, kv head, sequence) on the CUDA cores

@@ -766,6 +766,80 @@ __global__ void __launch_bounds__(256) decode_combine_spans_kernel(Params p) {
   if (p.lse != nullptr && lane == 0) p.lse[row] = (M + log2f(l)) * 0.69314718055994531f;
 }
 
+// The same merge with one block of 8 warps per (b, h), for launches whose
+// streams are few and long (one sequence of 131k tokens: ~111 pieces per
+// stream), where one warp per head would leave most SMs idle and walk its
+// pieces one by one: warp w takes pieces w, w + 8, ... against the row's
+// maximum M, and the block adds the 8 partial sums.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) decode_combine_heads_kernel(Params p) {
+  constexpr int C = D / 32;  // output columns per lane
+  static_assert(C == 2 || C == 4, "D is 64 or 128");
+  __shared__ float red_o[8][D];
+  __shared__ float red_x[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = blockIdx.x;  // b * Hq + h
+  grid_dependency_wait();  // the partials and the plan come from the split kernel
+  grid_dependents_launch();
+  const int b = (int)(row / p.Hq), h = (int)(row - (long long)b * p.Hq);
+  const long long nb = p.plan[b + 1] - p.plan[b];  // sub-tiles of each stream of b
+  int n = 0;
+  if (nb > 0) {
+    const long long N = p.plan[p.B] * p.Hkv, W = p.plan[p.B + 1];
+    const long long s0 = p.plan[b] * p.Hkv + (long long)(h / (p.Hq / p.Hkv)) * nb;
+    n = (int)(span_owner(s0 + nb - 1, N, W) - span_owner(s0, N, W)) + 1;
+  }
+  T* o = reinterpret_cast<T*>(p.o) + row * D;
+  if (n == 0) {
+    for (int d = threadIdx.x; d < D; d += blockDim.x) store_out(o + d, 0.f);
+    if (p.lse != nullptr && threadIdx.x == 0) p.lse[row] = -INFINITY;
+    return;
+  }
+  const float* wm = p.ws_m + row * p.splits;
+  const float* wl = p.ws_l + row * p.splits;
+  const float* wo = p.ws_o + row * p.splits * D + lane * C;
+  float M = -INFINITY;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) M = fmaxf(M, wm[i]);
+  M = warp_max(M);
+  if (lane == 0) red_x[warp] = M;
+  __syncthreads();
+  M = red_x[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) M = fmaxf(M, red_x[w]);
+  __syncthreads();  // red_x is reused below
+  float acc[C], l = 0.f;
+#pragma unroll
+  for (int c = 0; c < C; ++c) acc[c] = 0.f;
+  for (int i = warp; i < n; i += 8) {
+    const float sc = exp2f(wm[i] - M);
+    l = fmaf(sc, wl[i], l);
+    const float* src = wo + (size_t)i * D;
+    if constexpr (C == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] = fmaf(sc, v.x, acc[0]); acc[1] = fmaf(sc, v.y, acc[1]);
+      acc[2] = fmaf(sc, v.z, acc[2]); acc[3] = fmaf(sc, v.w, acc[3]);
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] = fmaf(sc, v.x, acc[0]); acc[1] = fmaf(sc, v.y, acc[1]);
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < C; ++c) red_o[warp][lane * C + c] = acc[c];
+  if (lane == 0) red_x[warp] = l;
+  __syncthreads();
+  float lt = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) lt += red_x[w];
+  const float inv = 1.f / lt;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float x = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) x += red_o[w][d];
+    store_out(o + d, x * inv);
+  }
+  if (p.lse != nullptr && threadIdx.x == 0) p.lse[row] = (M + log2f(lt)) * 0.69314718055994531f;
+}
+
 // Merge the chunk partials of the fp32 split kernel (one per 256-key chunk)
 // of one (b, h): grid (Hq, B), D threads.
 template <typename T, int D>

@@ -265,6 +265,25 @@ def test_decode_group_sizes_at_scale(E, cfg):
     compare(o, lse, ro, rl, d["q"].dtype, f"decode {cfg}")
 
 
+@pytest.mark.parametrize("cfg", [(1, 32, 8, 128, 131071, "bf16"), (2, 16, 2, 64, 60000, "f16"),
+                                 (3, 8, 1, 128, 20000, "bf16")],
+                         ids=["B1-131k-D128", "B2-60k-D64-f16", "B3-20k-G8"])
+def test_decode_few_long_streams(E, cfg):
+    """Decode of a few long sequences, where every stream is cut into many
+    pieces (up to ~111 per stream) and the merge runs one block per head:
+    every output against the oracle, through attn_decode_append (the new
+    token's rows written by the split kernel)."""
+    B, Hq, Hkv, D, n, dtype = cfg
+    d = workloads.decode_inputs(B, Hq, Hkv, D, n // 2, n, dtype, seed=71, device="cuda")
+    scale = 1.0 / math.sqrt(D)
+    o, lse = E.attn_decode_append(d["q"], d["kcache"], d["vcache"], d["k_new"], d["v_new"],
+                                  d["kv_len"], scale=scale)
+    torch.cuda.synchronize()
+    assert E.attn_device_error(clear=True) == 0
+    ro, rl = oracle_decode(d["q"], d["kcache"], d["vcache"], d["kv_len"], scale)
+    compare(o, lse, ro, rl, d["q"].dtype, f"decode {cfg}")
+
+
 def test_fp32_prefill_larger(E):
     """The exact fp32 path over several hundred blocks, causal with padding."""
     x = workloads.prefill_inputs(2, 4, 2, 700, 700, 128, "f32", seed=68, device="cuda",
