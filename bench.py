@@ -81,8 +81,8 @@ PROFILED_TRAFFIC = {
     5: {"source": "exact_tiled_attention_49_b300/csrc/fwd_bf16_tc.cuh", "sha256": "103911b9e59f",
         "bytes": 1082.855168e6 + 90.0608e6, "scale": 1.0,
         "capture": "fwd_bf16_tc_kernel<128,0,0>, full workload"},
-    4: {"source": "exact_tiled_attention_49_b300/csrc/decode.cuh", "sha256": "830803044526",
-        "bytes": 1339.822336e6 + 4.527872e6 + 3.423744e6, "scale": 1.0,
+    4: {"source": "exact_tiled_attention_49_b300/csrc/decode.cuh", "sha256": "69704c0ae728",
+        "bytes": 1339.805952e6 + 4.4928e6 + 3.42272e6, "scale": 1.0,
         "capture": "decode_split_mma_kernel<128,4,0> (append fused) + "
                    "decode_combine_spans_kernel, full workload"},
 }
